@@ -1,0 +1,127 @@
+/*
+ * h3gqa: bf16 causal grouped-query attention prefill for long sequences on
+ * GB300 (sm_103a). C ABI.
+ *
+ * The operation. antirez/h3.c issue #47 ("Qwen layer 0 causal GQA failed:
+ * causal attention sequence 10231 exceeds threadgroup memory"), sections
+ * "Error" and "Suggested fix directions": the causal grouped-query attention
+ * of the Qwen text encoder's prefill, whose Metal kernel keeps a query's whole
+ * fp32 score row on chip and so refuses sequences above about 7700 tokens.
+ * This library computes the same step with no bound on the sequence length
+ * from on-chip memory:
+ *
+ *   for each packed sequence b (token rows [cu[b], cu[b+1])),
+ *   for each query head h, key/value head g = h / (n_q_heads / n_kv_heads),
+ *   for each query row i of b:
+ *     z_j      = scale * <q[h,i,:], k[g,j,:]>    for keys j of b with j <= i
+ *     o[h,i,:] = sum_j softmax_j(z) * v[g,j,:]
+ *     lse[h,i] = ln sum_j exp(z_j)
+ *
+ * Layouts (all contiguous, head-major, the "[head,row,dimension]" attention
+ * order that the h3.c README gives in its "Profiling and diagnostic paths"
+ * section):
+ *   q, o : [n_q_heads][T][head_dim] bf16     T = cu_seqlens[n_seqs]
+ *   k, v : [n_kv_heads][T][head_dim] bf16
+ *   lse  : [n_q_heads][T] fp32 (natural log)
+ *
+ * Ownership and threading. The caller owns every buffer. Calls allocate no
+ * device memory and keep no per-call state. Work is queued on `stream` and
+ * the call returns without waiting for it. Calls on different streams may
+ * run concurrently as long as their outputs do not overlap.
+ *
+ * Errors. Every entry point returns a status and never exits or aborts the
+ * process. Argument checks run on the host before any CUDA call. A kernel
+ * whose internal pipeline waits exceed their iteration bound stops, frees
+ * what it holds and raises a device-side flag; h3gqa_sync_and_check reports
+ * it as H3GQA_ERR_TIMEOUT.
+ */
+#ifndef H3GQA_H_
+#define H3GQA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; 0 is the legacy default stream. */
+typedef struct CUstream_st *h3gqa_stream_t;
+
+typedef enum {
+    H3GQA_OK = 0,
+    H3GQA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad cu_seqlens, bad scale, heads */
+    H3GQA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim != 128, group size, too many sequences */
+    H3GQA_ERR_ARCH = 3,          /* current device is not compute capability 10.3 */
+    H3GQA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    H3GQA_ERR_TIMEOUT = 5        /* a kernel gave up on a bounded internal wait */
+} h3gqa_status;
+
+/*
+ * Causal GQA forward (the step of issue #47, "Error"; definition above).
+ *
+ *   q, k, v     device pointers, bf16, layouts above, 16-byte aligned.
+ *   o           device pointer, bf16 [n_q_heads][T][head_dim], 16-byte aligned.
+ *   lse         device pointer, fp32 [n_q_heads][T], 4-byte aligned.
+ *   cu_seqlens  HOST pointer to n_seqs + 1 int32: cu[0] = 0, non-decreasing,
+ *               cu[n_seqs] = T. Zero-length sequences are allowed. A single
+ *               sequence of length S is {0, S}.
+ *   n_seqs      number of packed sequences (>= 0; at most 1024 non-empty).
+ *   n_q_heads, n_kv_heads   n_q_heads = G * n_kv_heads with G a power of two,
+ *               2 <= G <= 128 (query head h reads KV head h / G).
+ *   head_dim    must be 128.
+ *   scale       multiplies the logits; finite and > 0 (e.g. 1/sqrt(128)).
+ *   stream      stream to queue the kernel on.
+ *
+ * Returns H3GQA_OK once the kernel is queued (T = 0 queues nothing).
+ * Invalid arguments return before any CUDA call. There is no limit on the
+ * sequence length other than T < 2^31 - 256 (TMA coordinates are int32).
+ * Rows of o/lse are written only for tokens inside some sequence, i.e. all
+ * of [0, T).
+ */
+h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v,
+                              void *o, float *lse,
+                              const int32_t *cu_seqlens, int n_seqs,
+                              int n_q_heads, int n_kv_heads, int head_dim,
+                              float scale, h3gqa_stream_t stream);
+
+/* Work plan of one h3gqa_causal_fwd call, computed on the host only (no GPU
+ * needed). A unit is (sequence, block of 256/G tokens, KV head); it owns two
+ * 128-row query tiles (G heads x 128/G tokens each) and visits every 128-key
+ * tile at or before its last token. */
+typedef struct {
+    int64_t total_tokens;       /* T */
+    int64_t n_units;            /* work units */
+    int64_t n_kv_tiles;         /* sum over units of 128-key tiles visited */
+    double tensor_flops;        /* FLOPs the MMAs execute: n_kv_tiles * 2 tiles * 2 GEMMs * 2*128^3 */
+    double causal_flops;        /* needed FLOPs: sum_b 2*Hq*D*S_b*(S_b+1) */
+    double metric_flops;        /* headline count: sum_b 2*Hq*D*S_b^2 */
+    double exp2_count;          /* needed exponentials: sum_b Hq*S_b*(S_b+1)/2 */
+    double algorithmic_bytes;   /* q,k,v read once + o,lse written once */
+    int32_t tokens_per_unit;    /* 256 / G */
+    int32_t max_kv_tiles;       /* most 128-key tiles any unit visits */
+} h3gqa_plan;
+
+/* Fills *plan for the given shape; same argument rules as h3gqa_causal_fwd
+ * (pointers and scale are not involved). Returns the status that
+ * h3gqa_causal_fwd would return for these sizes, without touching CUDA. */
+h3gqa_status h3gqa_make_plan(const int32_t *cu_seqlens, int n_seqs,
+                             int n_q_heads, int n_kv_heads, int head_dim,
+                             h3gqa_plan *plan);
+
+/* Waits for `stream`, then reads and clears the current device's timeout
+ * flag. Returns H3GQA_ERR_TIMEOUT if any kernel of this library on this
+ * device gave up on a bounded wait since the last check, H3GQA_ERR_CUDA if
+ * the synchronisation failed, else H3GQA_OK. */
+h3gqa_status h3gqa_sync_and_check(h3gqa_stream_t stream);
+
+/* Static description of a status code. */
+const char *h3gqa_status_string(h3gqa_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int h3gqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3GQA_H_ */

@@ -1,0 +1,146 @@
+"""Python binding of the h3gqa C ABI (include/h3gqa.h).
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library. Importing this module does not load the library; the first call
+does, and it raises if libh3gqa.so has not been built. There is no CPU
+fallback.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libh3gqa.so")
+
+H3GQA_OK = 0
+H3GQA_ERR_INVALID_ARG = 1
+H3GQA_ERR_UNSUPPORTED = 2
+H3GQA_ERR_ARCH = 3
+H3GQA_ERR_CUDA = 4
+H3GQA_ERR_TIMEOUT = 5
+
+EXPORTED = ("h3gqa_causal_fwd", "h3gqa_make_plan", "h3gqa_sync_and_check",
+            "h3gqa_status_string", "h3gqa_version")
+
+
+class H3GQAError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = int(status)
+        super().__init__("%s failed: %s (status %d)"
+                         % (where, h3gqa_status_string(status), self.status))
+
+
+class h3gqa_plan(ctypes.Structure):
+    _fields_ = [
+        ("total_tokens", ctypes.c_int64),
+        ("n_units", ctypes.c_int64),
+        ("n_kv_tiles", ctypes.c_int64),
+        ("tensor_flops", ctypes.c_double),
+        ("causal_flops", ctypes.c_double),
+        ("metric_flops", ctypes.c_double),
+        ("exp2_count", ctypes.c_double),
+        ("algorithmic_bytes", ctypes.c_double),
+        ("tokens_per_unit", ctypes.c_int32),
+        ("max_kv_tiles", ctypes.c_int32),
+    ]
+
+
+_LIB = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once) and declare the signatures of include/h3gqa.h."""
+    global _LIB
+    if _LIB is not None and path == LIB_PATH:
+        return _LIB
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built; run __graft_entry__.build() (needs nvcc)" % path)
+    lib = ctypes.CDLL(path)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    vp = ctypes.c_void_p
+    lib.h3gqa_causal_fwd.argtypes = [vp, vp, vp, vp, vp, i32p, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
+    lib.h3gqa_causal_fwd.restype = ctypes.c_int
+    lib.h3gqa_make_plan.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.POINTER(h3gqa_plan)]
+    lib.h3gqa_make_plan.restype = ctypes.c_int
+    lib.h3gqa_sync_and_check.argtypes = [vp]
+    lib.h3gqa_sync_and_check.restype = ctypes.c_int
+    lib.h3gqa_status_string.argtypes = [ctypes.c_int]
+    lib.h3gqa_status_string.restype = ctypes.c_char_p
+    lib.h3gqa_version.argtypes = []
+    lib.h3gqa_version.restype = ctypes.c_int
+    if path == LIB_PATH:
+        _LIB = lib
+    return lib
+
+
+def _cu_array(cu_seqlens):
+    vals = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    arr = (ctypes.c_int32 * max(len(vals), 1))(*vals)
+    return arr, len(vals) - 1
+
+
+def h3gqa_status_string(status) -> str:
+    return load().h3gqa_status_string(int(status)).decode()
+
+
+def h3gqa_version() -> int:
+    return int(load().h3gqa_version())
+
+
+def h3gqa_make_plan(cu_seqlens, n_q_heads, n_kv_heads, head_dim=128):
+    """Host-only work plan (see include/h3gqa.h). Raises H3GQAError on a bad shape."""
+    arr, n = _cu_array(cu_seqlens)
+    plan = h3gqa_plan()
+    st = load().h3gqa_make_plan(arr, n, int(n_q_heads), int(n_kv_heads), int(head_dim),
+                                ctypes.byref(plan))
+    if st != H3GQA_OK:
+        raise H3GQAError(st, "h3gqa_make_plan")
+    return plan
+
+
+def h3gqa_causal_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, cu_seqlens, n_q_heads, n_kv_heads,
+                     head_dim, scale, stream=0, check=True):
+    """Raw call: device pointers as ints, cu_seqlens host-side, stream handle as int.
+    Returns the status; raises H3GQAError on a non-zero status when check=True."""
+    arr, n = _cu_array(cu_seqlens)
+    st = load().h3gqa_causal_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, arr, n, int(n_q_heads),
+                                 int(n_kv_heads), int(head_dim), ctypes.c_float(scale),
+                                 stream or None)
+    if check and st != H3GQA_OK:
+        raise H3GQAError(st, "h3gqa_causal_fwd")
+    return st
+
+
+def h3gqa_sync_and_check(stream=0, check=True):
+    st = load().h3gqa_sync_and_check(stream or None)
+    if check and st != H3GQA_OK:
+        raise H3GQAError(st, "h3gqa_sync_and_check")
+    return st
+
+
+def causal_gqa_fwd(q, k, v, cu_seqlens, scale=None, o=None, lse=None, stream=None):
+    """Torch front end: q [Hq,T,D], k/v [Hkv,T,D] bf16 CUDA tensors (contiguous),
+    cu_seqlens host ints. Returns (o [Hq,T,D] bf16, lse [Hq,T] fp32) on q's device,
+    queued on `stream` (default: torch's current stream)."""
+    import torch
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be [heads, T, head_dim]")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bf16 CUDA tensor" % name)
+    hq, T, d = q.shape
+    hkv = k.shape[0]
+    if k.shape != (hkv, T, d) or v.shape != (hkv, T, d):
+        raise ValueError("k and v must be [Hkv, T, D] with q's T and D")
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    h3gqa_causal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     cu_seqlens, hq, hkv, d, float(scale), stream.cuda_stream)
+    return o, lse

@@ -1,0 +1,511 @@
+// Causal GQA prefill forward for sm_103a: TMA-staged Q/K/V tiles, tcgen05
+// MMAs into tensor memory, fp32 online softmax in exp2 form, per-row LSE.
+//
+// The step is the causal grouped-query attention of antirez/h3.c issue #47
+// ("Qwen layer 0 causal GQA failed: causal attention sequence 10231 exceeds
+// threadgroup memory", "Error"). That issue's kernel keeps the whole fp32
+// score row on chip, which caps the sequence near 7700 tokens; its
+// "Suggested fix directions" propose tiling the score row. Here the score
+// row is never materialised: keys stream through 128-key tiles and the
+// softmax is carried online (running max, running sum, rescaled output), so
+// on-chip state per query row is O(tile) and there is no length bound.
+//
+// Work decomposition ("pack-GQA"): a query tile is 128 MMA rows made of the
+// G = Hq/Hkv query heads of one KV head times 128/G consecutive tokens (row
+// r = head (r / (128/G)), token (r % (128/G))). A unit is two such tiles
+// (256/G consecutive tokens) plus every 128-key tile at or before its last
+// token, so each K/V tile staged in shared memory feeds all G query heads.
+//
+// CTA roles (320 threads, one CTA per SM, persistent over units):
+//   warps 0-3  softmax for query tile 0 (thread = MMA row = TMEM lane)
+//   warps 4-7  softmax for query tile 1
+//   warp  8    TMA producer (one lane)
+//   warp  9    TMEM allocator and MMA issuer (one lane)
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
+// P (bf16, two per column) overwrites the first 64 columns of its S.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include "ptx_sm103a.cuh"
+
+namespace h3gqa {
+
+constexpr int kHeadDim = 128;
+constexpr int kRows = 128;                 // MMA M: query rows per tile
+constexpr int kKeys = 128;                 // keys per K/V tile
+constexpr int kStages = 4;                 // K/V ring depth (K and V take one stage each)
+constexpr int kMaxSeqs = 1024;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kSubTileBytes = 128 * 128;          // 128 rows x 64 bf16 (one 128-B swizzle span)
+constexpr uint32_t kTileBytes = 2 * kSubTileBytes;     // 128 rows x 128 bf16
+constexpr uint32_t kQOff = 0;                          // two query tiles
+constexpr uint32_t kKvOff = kQOff + 2 * kTileBytes;
+constexpr uint32_t kBarOff = kKvOff + kStages * kTileBytes;
+// barrier slots
+constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + kStages,
+              kBarSFull = 2 + 2 * kStages, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2,
+              kBarDrain = kBarOFull + 2, kNumBars = kBarDrain + 1;
+constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag
+constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if the max grew by > 2^8
+#ifndef H3GQA_WAIT_NS
+#define H3GQA_WAIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitNs = H3GQA_WAIT_NS;         // wall time before a pipeline wait gives up
+constexpr uint64_t kDrainNs = 2000000000ull;        // wall time allowed for in-flight copies to land
+
+// Device-side timeout record (per device, static): bit 0 producer, bit 1
+// MMA issuer, bit 2 softmax, bit 3 teardown drain.
+__device__ unsigned int g_timeout_flags;
+
+struct FwdParams {
+    CUtensorMap map_q;      // q [Hq][T][128], box {64, 128/G, G}
+    CUtensorMap map_k;      // k [Hkv][T][128], box {64, 128, 1}
+    CUtensorMap map_v;      // v [Hkv][T][128], box {64, 128, 1}
+    uint16_t *o;            // bf16 [Hq][T][128]
+    float *lse;             // fp32 [Hq][T]
+    long long total_tokens;
+    long long n_units;
+    int n_kv_heads;
+    int group;              // G = Hq / Hkv
+    int tile_tokens;        // 128 / G tokens per query tile
+    int tile_tokens_log2;
+    int unit_tokens;        // 2 * tile_tokens
+    int blocks_per_class;   // 128 / unit_tokens: units of one sequence that visit the same number of K/V tiles
+    int n_seqs;             // non-empty sequences, sorted by length (descending)
+    int c_max;              // most K/V tiles any unit visits
+    float scale_log2;       // scale * log2(e)
+    int seq_start[kMaxSeqs];
+    int seq_len[kMaxSeqs];
+};
+
+struct Unit {
+    int seq_start;
+    int seq_len;
+    int block;      // token block index inside the sequence
+    int kv_head;
+};
+
+// Walks the global longest-first unit order. Units are grouped by cost
+// class c (= K/V tiles visited, from c_max down to 1); inside a class by
+// sequence (longest first), then block, then KV head. Every role of a CTA
+// runs the same walk, so no schedule is stored anywhere.
+struct UnitWalker {
+    int c;
+    int i;
+    long long base;
+
+    __device__ __forceinline__ void init(const FwdParams &p)
+    {
+        c = p.c_max;
+        i = 0;
+        base = 0;
+    }
+
+    __device__ __forceinline__ int blocks_in_class(const FwdParams &p, int cls, int seq) const
+    {
+        const int nblk = (p.seq_len[seq] + p.unit_tokens - 1) / p.unit_tokens;
+        const int lo = (cls - 1) * p.blocks_per_class;
+        const int hi = min(cls * p.blocks_per_class, nblk);
+        return hi > lo ? hi - lo : 0;
+    }
+
+    // u must not decrease from one call to the next, and u < n_units.
+    __device__ __forceinline__ Unit seek(const FwdParams &p, long long u)
+    {
+        for (;;) {
+            const long long cnt = (long long)blocks_in_class(p, c, i) * p.n_kv_heads;
+            if (u < base + cnt) break;
+            base += cnt;
+            ++i;
+            if (i >= p.n_seqs || blocks_in_class(p, c, i) == 0) {
+                i = 0;
+                --c;
+            }
+        }
+        const long long j = u - base;
+        Unit r;
+        r.seq_start = p.seq_start[i];
+        r.seq_len = p.seq_len[i];
+        r.kv_head = (int)(j % p.n_kv_heads);
+        r.block = (c - 1) * p.blocks_per_class + (int)(j / p.n_kv_heads);
+        return r;
+    }
+};
+
+// Round r of the static schedule hands CTA x the unit r*grid + x on even
+// rounds and r*grid + (grid-1-x) on odd ones (a snake over the longest-first
+// order), which evens out the linearly falling unit costs.
+__device__ __forceinline__ long long unit_of_round(long long r)
+{
+    const long long g = gridDim.x;
+    const long long x = blockIdx.x;
+    return r * g + ((r & 1) ? (g - 1 - x) : x);
+}
+
+__device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int who)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t n = 0;
+    while (!mbar_try_wait_capped(bar, parity)) {
+        if (((++n) & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                atomicOr(&g_timeout_flags, who);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// Waits without giving up early on an abort (teardown: copies or MMAs in
+// flight must finish before the CTA releases its memory); bounded in time.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_capped(bar, parity)) {
+        if (global_timer_ns() - t0 > kDrainNs) {
+            atomicOr(&g_timeout_flags, 8u);
+            return false;
+        }
+    }
+    return true;
+}
+
+// All 32 lanes wait; the result is agreed across the warp so that the
+// .sync.aligned TMEM instructions after it never run on a partial warp.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int who)
+{
+    bool ok = wait_poll(bar, parity, abort_flag, who);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) *abort_flag = 1;
+    return ok;
+}
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr)
+{
+    // K-major operand, 128-B swizzle: 8-row groups 1024 B apart (SBO); the
+    // leading offset is unused for this layout.
+    return sdesc_sw128(saddr, 16, 1024);
+}
+
+__device__ __forceinline__ uint64_t vmn_desc(uint32_t saddr)
+{
+    // V as the MN-major B operand: 64 head dims per 128-B row, the next 64
+    // dims one sub-tile (16 KB) further (LBO), 8-key groups 1024 B apart (SBO).
+    return sdesc_sw128(saddr, kSubTileBytes, 1024);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t sQ = sbase + kQOff;
+    const uint32_t sKV = sbase + kKvOff;
+    auto bar = [&](int i) -> uint32_t { return sbase + kBarOff + 8u * (uint32_t)i; };
+    volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kBarQFull), 1);
+        mbar_init(bar(kBarQEmpty), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(kBarKvFull + s), 1);
+            mbar_init(bar(kBarKvEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(kBarSFull + t), 1);
+            mbar_init(bar(kBarPFull + t), kRows);
+            mbar_init(bar(kBarOFull + t), 1);
+        }
+        mbar_init(bar(kBarDrain), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(const_cast<uint32_t *>(misc)), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = misc[0];
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_map(&p.map_q);
+            tma_prefetch_map(&p.map_k);
+            tma_prefetch_map(&p.map_v);
+            UnitWalker w;
+            w.init(p);
+            uint32_t kv_it = 0, unit_it = 0;
+            int last_kv_parity[kStages];
+            for (int s = 0; s < kStages; ++s) last_kv_parity[s] = -1;
+            int last_q_parity = -1;
+            bool ok = true;
+            for (long long r = 0; ok; ++r) {
+                const long long u = unit_of_round(r);
+                if (u >= p.n_units) break;
+                const Unit un = w.seek(p, u);
+                const int tb = un.block * p.unit_tokens;
+                const int n_kv = tb / kKeys + 1;
+                if (!wait_poll(bar(kBarQEmpty), (unit_it & 1) ^ 1, abort_flag, 1u)) { ok = false; break; }
+                mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+                last_q_parity = unit_it & 1;
+                for (int t = 0; t < 2; ++t)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(sQ + (uint32_t)(t * 2 + h) * kSubTileBytes, &p.map_q,
+                                    bar(kBarQFull), 64 * h, un.seq_start + tb + t * p.tile_tokens,
+                                    un.kv_head * p.group);
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    for (int kind = 0; kind < 2; ++kind) {
+                        const uint32_t s = kv_it % kStages;
+                        const uint32_t ph = (kv_it / kStages) & 1;
+                        if (!wait_poll(bar(kBarKvEmpty + s), ph ^ 1, abort_flag, 1u)) { ok = false; break; }
+                        mbar_arrive_expect_tx(bar(kBarKvFull + s), kTileBytes);
+                        last_kv_parity[s] = (int)ph;
+                        const CUtensorMap *map = kind ? &p.map_v : &p.map_k;
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d(sKV + s * kTileBytes + (uint32_t)h * kSubTileBytes, map,
+                                        bar(kBarKvFull + s), 64 * h, un.seq_start + j * kKeys,
+                                        un.kv_head);
+                        ++kv_it;
+                    }
+                }
+                ++unit_it;
+            }
+            if (!ok) {
+                // Let every copy already issued land before the CTA exits.
+                for (int s = 0; s < kStages; ++s)
+                    if (last_kv_parity[s] >= 0) wait_drain(bar(kBarKvFull + s), (uint32_t)last_kv_parity[s]);
+                if (last_q_parity >= 0) wait_drain(bar(kBarQFull), (uint32_t)last_q_parity);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(kRows, kKeys, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(kRows, kHeadDim, true);
+            UnitWalker w;
+            w.init(p);
+            uint32_t kv_it = 0, unit_it = 0;
+            uint32_t p_phase[2] = {0, 0};
+            bool ok = true;
+
+            auto issue_s = [&](int t, uint32_t stage) {
+                const uint32_t a0 = sQ + (uint32_t)t * kTileBytes;
+                const uint32_t b0 = sKV + stage * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * kSubTileBytes + (uint32_t)(kk & 3) * 32u;
+                    mma_bf16_ss(tmem + (uint32_t)t * 128u, kmajor_desc(a0 + off), kmajor_desc(b0 + off),
+                                idS, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
+                const uint32_t b0 = sKV + stage * kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    mma_bf16_ts(tmem + 256u + (uint32_t)t * 128u, tmem + (uint32_t)t * 128u + (uint32_t)kk * 8u,
+                                vmn_desc(b0 + (uint32_t)kk * 2048u), idPV,
+                                (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            for (long long r = 0; ok; ++r) {
+                const long long u = unit_of_round(r);
+                if (u >= p.n_units) break;
+                const Unit un = w.seek(p, u);
+                const int n_kv = (un.block * p.unit_tokens) / kKeys + 1;
+                if (!wait_poll(bar(kBarQFull), unit_it & 1, abort_flag, 2u)) { ok = false; break; }
+                {
+                    const uint32_t s = kv_it % kStages;
+                    if (!wait_poll(bar(kBarKvFull + s), (kv_it / kStages) & 1, abort_flag, 2u)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    issue_s(0, s);
+                    mma_commit(bar(kBarSFull + 0));
+                    issue_s(1, s);
+                    mma_commit(bar(kBarSFull + 1));
+                    mma_commit(bar(kBarKvEmpty + s));
+                }
+                for (int j = 0; j < n_kv && ok; ++j) {
+                    const uint32_t itv = kv_it + 2u * j + 1u;
+                    const uint32_t sv = itv % kStages;
+                    const bool more = j + 1 < n_kv;
+                    const uint32_t itk = itv + 1u;
+                    const uint32_t sk = itk % kStages;
+                    if (!wait_poll(bar(kBarKvFull + sv), (itv / kStages) & 1, abort_flag, 2u)) { ok = false; break; }
+                    if (more && !wait_poll(bar(kBarKvFull + sk), (itk / kStages) & 1, abort_flag, 2u)) { ok = false; break; }
+                    for (int t = 0; t < 2; ++t) {
+                        if (!wait_poll(bar(kBarPFull + t), p_phase[t] & 1, abort_flag, 2u)) { ok = false; break; }
+                        ++p_phase[t];
+                        tc_fence_after_sync();
+                        issue_pv(t, sv, j > 0);
+                        if (more) {
+                            issue_s(t, sk);
+                            mma_commit(bar(kBarSFull + t));
+                        } else {
+                            mma_commit(bar(kBarOFull + t));
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(kBarKvEmpty + sv));
+                    if (more) mma_commit(bar(kBarKvEmpty + sk));
+                }
+                if (!ok) break;
+                mma_commit(bar(kBarQEmpty));
+                kv_it += 2u * (uint32_t)n_kv;
+                ++unit_it;
+            }
+            // Nothing issued may still be running when TMEM is freed.
+            mma_commit(bar(kBarDrain));
+            wait_drain(bar(kBarDrain), 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- softmax
+        const int t = warp >> 2;                 // query tile of this warpgroup
+        const int row = threadIdx.x - 128 * t;   // MMA row = TMEM lane
+        const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_bits + (uint32_t)t * 128u;
+        const uint32_t tO = tmem + lane_bits + 256u + (uint32_t)t * 128u;
+        const int head_in_group = row >> p.tile_tokens_log2;
+        const int tok_in_tile = row & (p.tile_tokens - 1);
+        const float c = p.scale_log2;
+        UnitWalker w;
+        w.init(p);
+        uint32_t s_phase = 0, o_phase = 0;
+        bool ok = true;
+        for (long long r = 0; ok; ++r) {
+            const long long u = unit_of_round(r);
+            if (u >= p.n_units) break;
+            const Unit un = w.seek(p, u);
+            const int tb = un.block * p.unit_tokens;
+            const int n_kv = tb / kKeys + 1;
+            const int tok = tb + t * p.tile_tokens + tok_in_tile;   // token inside its sequence
+            float m = -INFINITY;   // running max of the scaled logits, log2 units
+            float l = 0.f;         // running sum of exp2(logit - m)
+            for (int j = 0; j < n_kv; ++j) {
+                if (!wait_warp(bar(kBarSFull + t), s_phase & 1, abort_flag, 4u)) { ok = false; break; }
+                ++s_phase;
+                tc_fence_after_sync();
+                float s[kKeys];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t rr[32];
+                    tmem_ld32_wait(tS + (uint32_t)ch * 32u, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(rr[i]);
+                }
+                if (j == n_kv - 1) {
+                    // diagonal tile: key (j*128 + i) is visible iff it is <= tok
+                    const int lim = tok - j * kKeys;
+#pragma unroll
+                    for (int i = 0; i < kKeys; ++i)
+                        if (i > lim) s[i] = -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int i = 4; i < kKeys; i += 4) {
+                    mx0 = fmaxf(mx0, s[i]);
+                    mx1 = fmaxf(mx1, s[i + 1]);
+                    mx2 = fmaxf(mx2, s[i + 2]);
+                    mx3 = fmaxf(mx3, s[i + 3]);
+                }
+                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+                const float m_new = fmaxf(m, m_tile);
+                float m_use = m, alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_use = m_new;
+                } else if (m_new - m > kRescaleThreshold) {
+                    m_use = m_new;
+                    alpha = ex2_approx(m - m_new);
+                    rescale = true;
+                }
+                float sum0 = 0.f, sum1 = 0.f;
+                uint32_t pk[kKeys / 2];
+#pragma unroll
+                for (int i = 0; i < kKeys / 2; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[2 * i], c, -m_use));
+                    const float p1 = ex2_approx(fmaf(s[2 * i + 1], c, -m_use));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                l = l * alpha + (sum0 + sum1);
+                m = m_use;
+                tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+                tmem_st32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // PV of the previous tile is complete (it was issued
+                    // before this S), so O can be scaled in place.
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t rr[32];
+                        tmem_ld32_wait(tO + (uint32_t)ch * 32u, rr);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+                        tmem_st32(tO + (uint32_t)ch * 32u, rr);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(bar(kBarPFull + t));
+            }
+            if (!ok) break;
+            // ------------------------------------------------------ epilogue
+            if (!wait_warp(bar(kBarOFull + t), o_phase & 1, abort_flag, 4u)) { ok = false; break; }
+            ++o_phase;
+            tc_fence_after_sync();
+            const float inv_l = 1.0f / l;
+            const bool valid = tok < un.seq_len;
+            const long long grow = (long long)(un.kv_head * p.group + head_in_group) * p.total_tokens +
+                                   un.seq_start + tok;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * kHeadDim);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t rr[32];
+                tmem_ld32_wait(tO + (uint32_t)ch * 32u, rr);
+                if (valid) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 pkt;
+                        pkt.x = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 0]) * inv_l, __uint_as_float(rr[v4 * 8 + 1]) * inv_l);
+                        pkt.y = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 2]) * inv_l, __uint_as_float(rr[v4 * 8 + 3]) * inv_l);
+                        pkt.z = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 4]) * inv_l, __uint_as_float(rr[v4 * 8 + 5]) * inv_l);
+                        pkt.w = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 6]) * inv_l, __uint_as_float(rr[v4 * 8 + 7]) * inv_l);
+                        dst[ch * 4 + v4] = pkt;
+                    }
+                }
+            }
+            if (valid) p.lse[grow] = (m + __log2f(l)) * 0.69314718055994531f;
+            tc_fence_before_sync();
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace h3gqa

@@ -1,0 +1,284 @@
+// Host side of the h3gqa C ABI: argument checks, the work plan, TMA tensor
+// maps and the launch of the sm_103a causal GQA kernel.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/h3gqa.h"
+#include "fwd_kernel.cuh"
+
+namespace {
+
+using h3gqa::FwdParams;
+
+constexpr int kVersion = 10000;   // 1.0.0
+constexpr long long kMaxTotalTokens = (1LL << 31) - 256;
+
+struct HostPlan {
+    int group = 0;
+    int tile_tokens = 0;
+    int unit_tokens = 0;
+    int blocks_per_class = 0;
+    int c_max = 0;
+    long long n_units = 0;
+    long long n_kv_tiles = 0;
+    long long total_tokens = 0;
+    std::vector<int> start;   // non-empty sequences, longest first
+    std::vector<int> len;
+};
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int ilog2(int x)
+{
+    int r = 0;
+    while ((1 << r) < x) ++r;
+    return r;
+}
+
+// Shape checks shared by the plan query and the forward call; no CUDA.
+h3gqa_status build_plan(const int32_t *cu, int n_seqs, int hq, int hkv, int head_dim,
+                        HostPlan *out)
+{
+    if (cu == nullptr || n_seqs < 0) return H3GQA_ERR_INVALID_ARG;
+    if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return H3GQA_ERR_INVALID_ARG;
+    if (head_dim <= 0) return H3GQA_ERR_INVALID_ARG;
+    if (cu[0] != 0) return H3GQA_ERR_INVALID_ARG;
+    for (int b = 0; b < n_seqs; ++b)
+        if (cu[b + 1] < cu[b]) return H3GQA_ERR_INVALID_ARG;
+    if (head_dim != h3gqa::kHeadDim) return H3GQA_ERR_UNSUPPORTED;
+    const int g = hq / hkv;
+    if (!is_pow2(g) || g < 2 || g > h3gqa::kRows) return H3GQA_ERR_UNSUPPORTED;
+    const long long T = cu[n_seqs];
+    if (T > kMaxTotalTokens) return H3GQA_ERR_UNSUPPORTED;
+
+    HostPlan p;
+    p.group = g;
+    p.tile_tokens = h3gqa::kRows / g;
+    p.unit_tokens = 2 * p.tile_tokens;
+    p.blocks_per_class = h3gqa::kKeys / p.unit_tokens;
+    p.total_tokens = T;
+    std::vector<int> order;
+    for (int b = 0; b < n_seqs; ++b)
+        if (cu[b + 1] > cu[b]) order.push_back(b);
+    if ((int)order.size() > h3gqa::kMaxSeqs) return H3GQA_ERR_UNSUPPORTED;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        return (cu[a + 1] - cu[a]) > (cu[b + 1] - cu[b]);
+    });
+    for (int b : order) {
+        const int len = cu[b + 1] - cu[b];
+        p.start.push_back(cu[b]);
+        p.len.push_back(len);
+        const long long nblk = (len + p.unit_tokens - 1) / p.unit_tokens;
+        p.n_units += nblk * hkv;
+        // block k visits floor(k*unit/128) + 1 key tiles
+        for (long long k = 0; k < nblk; ++k)
+            p.n_kv_tiles += (k * p.unit_tokens / h3gqa::kKeys + 1) * hkv;
+    }
+    if (!p.len.empty()) {
+        const long long nblk0 = (p.len[0] + p.unit_tokens - 1) / p.unit_tokens;
+        p.c_max = (int)((nblk0 + p.blocks_per_class - 1) / p.blocks_per_class);
+    }
+    *out = std::move(p);
+    return H3GQA_OK;
+}
+
+// ------------------------------------------------------------ per device
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+    bool ready = false;
+    h3gqa_status status = H3GQA_OK;
+    int sm_count = 0;
+};
+
+std::mutex g_mutex;
+std::vector<DeviceState> g_devices;
+EncodeTiledFn g_encode = nullptr;
+
+h3gqa_status device_setup(int dev, DeviceState **out)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if ((int)g_devices.size() <= dev) g_devices.resize(dev + 1);
+    DeviceState &d = g_devices[dev];
+    if (d.ready) {
+        *out = &d;
+        return d.status;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return H3GQA_ERR_CUDA;
+    d.ready = true;
+    d.sm_count = sms;
+    if (major != 10 || minor != 3) {
+        d.status = H3GQA_ERR_ARCH;
+        *out = &d;
+        return d.status;
+    }
+    if (cudaFuncSetAttribute(h3gqa::causal_gqa_fwd_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)h3gqa::kSmemBytes) != cudaSuccess) {
+        d.ready = false;
+        return H3GQA_ERR_CUDA;
+    }
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+            d.ready = false;
+            return H3GQA_ERR_CUDA;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.status = H3GQA_OK;
+    *out = &d;
+    return H3GQA_OK;
+}
+
+// A [heads][T][128] bf16 tensor as a 3-D TMA map with a {64, rows, heads}
+// box and the 128-byte swizzle that the tcgen05 descriptors expect.
+bool encode_map(CUtensorMap *map, const void *base, int heads, long long T,
+                int box_rows, int box_heads)
+{
+    cuuint64_t dims[3] = {(cuuint64_t)h3gqa::kHeadDim, (cuuint64_t)T, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)h3gqa::kHeadDim * 2,
+                             (cuuint64_t)T * h3gqa::kHeadDim * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_heads};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+h3gqa_status h3gqa_make_plan(const int32_t *cu_seqlens, int n_seqs, int n_q_heads,
+                             int n_kv_heads, int head_dim, h3gqa_plan *plan)
+{
+    if (plan == nullptr) return H3GQA_ERR_INVALID_ARG;
+    HostPlan hp;
+    const h3gqa_status st = build_plan(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim, &hp);
+    if (st != H3GQA_OK) return st;
+    std::memset(plan, 0, sizeof(*plan));
+    plan->total_tokens = hp.total_tokens;
+    plan->n_units = hp.n_units;
+    plan->n_kv_tiles = hp.n_kv_tiles;
+    plan->tensor_flops = (double)hp.n_kv_tiles * 2.0 * 2.0 * 2.0 * 128.0 * 128.0 * 128.0;
+    double causal = 0, metric = 0, ex = 0;
+    for (int s : hp.len) {
+        causal += 2.0 * n_q_heads * head_dim * (double)s * (double)(s + 1);
+        metric += 2.0 * n_q_heads * head_dim * (double)s * (double)s;
+        ex += (double)n_q_heads * (double)s * (double)(s + 1) / 2.0;
+    }
+    plan->causal_flops = causal;
+    plan->metric_flops = metric;
+    plan->exp2_count = ex;
+    const double T = (double)hp.total_tokens;
+    plan->algorithmic_bytes = 2.0 * T * head_dim * (2.0 * n_q_heads + 2.0 * n_kv_heads) +
+                              4.0 * T * n_q_heads;
+    plan->tokens_per_unit = hp.unit_tokens;
+    plan->max_kv_tiles = hp.c_max;
+    return H3GQA_OK;
+}
+
+h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int n_seqs, int n_q_heads,
+                              int n_kv_heads, int head_dim, float scale, h3gqa_stream_t stream)
+{
+    if (!q || !k || !v || !o || !lse) return H3GQA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4))
+        return H3GQA_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return H3GQA_ERR_INVALID_ARG;
+    HostPlan hp;
+    h3gqa_status st = build_plan(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim, &hp);
+    if (st != H3GQA_OK) return st;
+    if (hp.n_units == 0) return H3GQA_OK;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return H3GQA_ERR_CUDA;
+    DeviceState *ds = nullptr;
+    st = device_setup(dev, &ds);
+    if (st != H3GQA_OK) return st;
+
+    FwdParams *prm = new (std::nothrow) FwdParams;
+    if (prm == nullptr) return H3GQA_ERR_CUDA;
+    std::memset(prm, 0, sizeof(*prm));
+    const long long T = hp.total_tokens;
+    if (!encode_map(&prm->map_q, q, n_q_heads, T, hp.tile_tokens, hp.group) ||
+        !encode_map(&prm->map_k, k, n_kv_heads, T, h3gqa::kKeys, 1) ||
+        !encode_map(&prm->map_v, v, n_kv_heads, T, h3gqa::kKeys, 1)) {
+        delete prm;
+        return H3GQA_ERR_CUDA;
+    }
+    prm->o = static_cast<uint16_t *>(o);
+    prm->lse = lse;
+    prm->total_tokens = T;
+    prm->n_units = hp.n_units;
+    prm->n_kv_heads = n_kv_heads;
+    prm->group = hp.group;
+    prm->tile_tokens = hp.tile_tokens;
+    prm->tile_tokens_log2 = ilog2(hp.tile_tokens);
+    prm->unit_tokens = hp.unit_tokens;
+    prm->blocks_per_class = hp.blocks_per_class;
+    prm->n_seqs = (int)hp.len.size();
+    prm->c_max = hp.c_max;
+    prm->scale_log2 = scale * 1.4426950408889634f;
+    for (size_t i = 0; i < hp.len.size(); ++i) {
+        prm->seq_start[i] = hp.start[i];
+        prm->seq_len[i] = hp.len[i];
+    }
+    const long long grid = std::min<long long>(hp.n_units, ds->sm_count);
+    h3gqa::causal_gqa_fwd_kernel<<<(unsigned)grid, h3gqa::kThreads, h3gqa::kSmemBytes,
+                                   reinterpret_cast<cudaStream_t>(stream)>>>(*prm);
+    delete prm;
+    return cudaGetLastError() == cudaSuccess ? H3GQA_OK : H3GQA_ERR_CUDA;
+}
+
+h3gqa_status h3gqa_sync_and_check(h3gqa_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return H3GQA_ERR_CUDA;
+    unsigned int flags = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&flags, h3gqa::g_timeout_flags, sizeof(flags)) != cudaSuccess)
+        return H3GQA_ERR_CUDA;
+    if (flags != 0 &&
+        cudaMemcpyToSymbol(h3gqa::g_timeout_flags, &zero, sizeof(zero)) != cudaSuccess)
+        return H3GQA_ERR_CUDA;
+    return flags ? H3GQA_ERR_TIMEOUT : H3GQA_OK;
+}
+
+const char *h3gqa_status_string(h3gqa_status s)
+{
+    switch (s) {
+    case H3GQA_OK: return "ok";
+    case H3GQA_ERR_INVALID_ARG: return "invalid argument";
+    case H3GQA_ERR_UNSUPPORTED: return "unsupported shape (head_dim must be 128, Hq/Hkv a power of two in [2,128], at most 1024 non-empty sequences)";
+    case H3GQA_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+    case H3GQA_ERR_CUDA: return "CUDA call failed";
+    case H3GQA_ERR_TIMEOUT: return "kernel gave up on a bounded internal wait";
+    }
+    return "unknown status";
+}
+
+int h3gqa_version(void) { return kVersion; }
+
+}  // extern "C"

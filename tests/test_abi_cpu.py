@@ -1,0 +1,145 @@
+"""The C-ABI library loads, exports what include/h3gqa.h declares, and checks
+its arguments on the host (CPU only: no call here reaches CUDA)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from long_causal_gqa_gb300 import binding, build
+from long_causal_gqa_gb300.binding import (H3GQA_ERR_INVALID_ARG, H3GQA_ERR_UNSUPPORTED,
+                                           H3GQA_OK, H3GQAError)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "h3gqa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(h3gqa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in _declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "h3gqa.h"\nint main(void){return h3gqa_version() > 0 ? 0 : 1;}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-c", "-I",
+                    os.path.join(ROOT, "include"), str(src), "-o", str(tmp_path / "use.o")],
+                   check=True)
+
+
+def test_version_and_status_strings(lib):
+    assert binding.h3gqa_version() == 10000
+    for st in range(6):
+        assert binding.h3gqa_status_string(st)
+    assert binding.h3gqa_status_string(99) == "unknown status"
+
+
+def test_plan_headline_shape(lib):
+    p = binding.h3gqa_make_plan([0, 10231], 64, 8, 128)
+    assert p.total_tokens == 10231
+    assert p.tokens_per_unit == 32                   # two tiles of 16 tokens x 8 heads
+    assert p.n_units == 320 * 8                      # ceil(10231/32) blocks x 8 KV heads
+    # block k visits floor(k/4)+1 key tiles: 8 heads * 4 * (1+...+80)
+    assert p.n_kv_tiles == 8 * 4 * (80 * 81 // 2)
+    assert p.max_kv_tiles == 80
+    assert p.metric_flops == 2.0 * 10231 ** 2 * 64 * 128
+    assert p.causal_flops == 2.0 * 64 * 128 * 10231 * 10232
+    assert p.exp2_count == 64 * 10231 * 10232 / 2
+    assert p.tensor_flops == p.n_kv_tiles * 8 * 128 ** 3
+    # the MMAs do the needed work plus the masked part of the diagonal tiles
+    assert 1.0 < p.tensor_flops / p.causal_flops < 1.03
+    t = 10231
+    assert p.algorithmic_bytes == 2 * t * 128 * (2 * 64 + 2 * 8) + 4 * t * 64
+
+
+def test_plan_varlen_and_groups(lib):
+    p = binding.h3gqa_make_plan([0, 8184, 16383, 24893, 35124], 64, 8)
+    assert p.total_tokens == 35124
+    assert p.n_units == 8 * sum((s + 31) // 32 for s in (8184, 8199, 8510, 10231))
+    p2 = binding.h3gqa_make_plan([0, 0, 5, 5], 16, 8)         # G = 2: 64 tokens per tile
+    assert p2.tokens_per_unit == 128 and p2.n_units == 8 and p2.max_kv_tiles == 1
+    p3 = binding.h3gqa_make_plan([0, 300], 128, 1)            # G = 128: one token per tile
+    assert p3.tokens_per_unit == 2 and p3.n_units == 150
+    p0 = binding.h3gqa_make_plan([0], 64, 8)
+    assert p0.n_units == 0 and p0.total_tokens == 0
+
+
+@pytest.mark.parametrize("cu,hq,hkv,d,status", [
+    ([1, 5], 64, 8, 128, H3GQA_ERR_INVALID_ARG),       # cu[0] != 0
+    ([0, 5, 3], 64, 8, 128, H3GQA_ERR_INVALID_ARG),    # decreasing
+    ([0, 5], 64, 7, 128, H3GQA_ERR_INVALID_ARG),       # Hq % Hkv != 0
+    ([0, 5], 0, 8, 128, H3GQA_ERR_INVALID_ARG),
+    ([0, 5], 64, 8, 0, H3GQA_ERR_INVALID_ARG),
+    ([0, 5], 64, 8, 64, H3GQA_ERR_UNSUPPORTED),        # head_dim
+    ([0, 5], 8, 8, 128, H3GQA_ERR_UNSUPPORTED),        # G = 1
+    ([0, 5], 24, 8, 128, H3GQA_ERR_UNSUPPORTED),       # G = 3
+    ([0, 5], 256, 1, 128, H3GQA_ERR_UNSUPPORTED),      # G = 256
+])
+def test_plan_rejects(lib, cu, hq, hkv, d, status):
+    with pytest.raises(H3GQAError) as e:
+        binding.h3gqa_make_plan(cu, hq, hkv, d)
+    assert e.value.status == status
+
+
+def test_too_many_sequences_unsupported(lib):
+    cu = list(range(0, 1026))          # 1025 sequences of length 1
+    with pytest.raises(H3GQAError) as e:
+        binding.h3gqa_make_plan(cu, 64, 8)
+    assert e.value.status == H3GQA_ERR_UNSUPPORTED
+    cu2 = [0] * 3000 + list(range(1, 1025))   # zero-length ones do not count
+    assert binding.h3gqa_make_plan(cu2, 64, 8).n_units == 1024 * 8
+
+
+def test_forward_rejects_before_touching_cuda(lib):
+    good = 1 << 20   # fake, 16-byte aligned "device" addresses; never dereferenced
+    args = dict(q_ptr=good, k_ptr=good, v_ptr=good, o_ptr=good, lse_ptr=good,
+                cu_seqlens=[0, 64], n_q_heads=64, n_kv_heads=8, head_dim=128, scale=0.088)
+    for bad in (dict(q_ptr=0), dict(o_ptr=good + 8), dict(lse_ptr=good + 2),
+                dict(scale=0.0), dict(scale=-1.0), dict(scale=float("inf")),
+                dict(scale=float("nan")), dict(cu_seqlens=[0, 64, 32])):
+        a = dict(args, **bad)
+        st = binding.h3gqa_causal_fwd(check=False, **a)
+        assert st == H3GQA_ERR_INVALID_ARG, bad
+    st = binding.h3gqa_causal_fwd(check=False, **dict(args, head_dim=64))
+    assert st == H3GQA_ERR_UNSUPPORTED
+    # T = 0 is a no-op and needs no device
+    assert binding.h3gqa_causal_fwd(check=False, **dict(args, cu_seqlens=[0, 0])) == H3GQA_OK
+    assert binding.h3gqa_causal_fwd(check=False, **dict(args, cu_seqlens=[0])) == H3GQA_OK
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load(str(tmp_path / "missing.so"))
+
+
+def test_library_links_no_oracle():
+    out = subprocess.run(["nm", "-D", binding.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    assert "oracle" not in out
+    src_dir = os.path.join(ROOT, "long_causal_gqa_gb300")
+    for dirpath, _, files in os.walk(src_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                assert "oracle" not in open(os.path.join(dirpath, f)).read().lower() or \
+                    f == "inputs.py", f

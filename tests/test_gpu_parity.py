@@ -1,0 +1,161 @@
+"""GPU parity: the sm_103a library against the fp64 oracle, element by element.
+
+Bar (the acceptance rule of the causal GQA target): every output element
+|o - ref| <= 1e-2 + 1e-2*|ref|, every LSE |lse - ref| <= 1e-3 (natural log).
+Small shapes are checked in full; the full-size workloads on sampled rows
+that the oracle computes one by one (first/last rows of every sequence, rows
+on both sides of every 128-token boundary, and seeded random rows), all
+heads. Output buffers carry guard regions that must come back untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+from long_causal_gqa_gb300 import binding
+from long_causal_gqa_gb300.inputs import WORKLOADS, make_inputs, make_workload_inputs
+from oracle import causal_gqa as orc
+
+pytestmark = pytest.mark.gpu
+
+O_ATOL, O_RTOL, LSE_ATOL = 1e-2, 1e-2, 1e-3
+GUARD = 4096
+O_SENTINEL = -12345      # int16 bit pattern written around o
+LSE_SENTINEL = 0x7FBADBAD  # int32 NaN pattern written around lse
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    binding.load()
+    return torch.device("cuda:0")
+
+
+def run_gpu(x, hq, hkv, scale, dev, stream=None):
+    """Runs the library with guard regions around o and lse; returns numpy
+    (o fp64 [Hq,T,D], lse fp64 [Hq,T])."""
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    T, d = q.shape[1], q.shape[2]
+    n_o, n_l = hq * T * d, hq * T
+    o_buf = torch.full((n_o + 2 * GUARD,), O_SENTINEL, dtype=torch.int16, device=dev)
+    l_buf = torch.full((n_l + 2 * GUARD,), LSE_SENTINEL, dtype=torch.int32, device=dev)
+    o = o_buf[GUARD:GUARD + n_o].view(torch.bfloat16).view(hq, T, d)
+    lse = l_buf[GUARD:GUARD + n_l].view(torch.float32).view(hq, T)
+    s = stream or torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    binding.causal_gqa_fwd(q, k, v, x["cu_seqlens"], scale, o=o, lse=lse, stream=s)
+    binding.h3gqa_sync_and_check(s.cuda_stream)
+    ob, lb = o_buf.cpu(), l_buf.cpu()
+    for name, buf, sent in (("o", ob, O_SENTINEL), ("lse", lb, LSE_SENTINEL)):
+        assert (buf[:GUARD] == sent).all() and (buf[-GUARD:] == sent).all(), \
+            "write outside %s" % name
+    return (o.float().cpu().numpy().astype(np.float64),
+            lse.cpu().numpy().astype(np.float64))
+
+
+def assert_close(o, lse, ref_o, ref_lse, what=""):
+    assert np.isfinite(o).all(), "non-finite o %s" % what
+    assert np.isfinite(lse).all(), "non-finite lse %s" % what
+    excess = np.abs(o - ref_o) - (O_ATOL + O_RTOL * np.abs(ref_o))
+    if excess.max() > 0:
+        idx = np.unravel_index(np.argmax(excess), excess.shape)
+        bad = (excess > 0).sum()
+        raise AssertionError("o mismatch %s: %d elements over tolerance; worst at %s: got %r "
+                             "want %r" % (what, bad, idx, o[idx], ref_o[idx]))
+    lerr = np.abs(lse - ref_lse)
+    if lerr.max() > LSE_ATOL:
+        idx = np.unravel_index(np.argmax(lerr), lerr.shape)
+        raise AssertionError("lse mismatch %s: %d over tolerance; worst at %s: got %r want %r"
+                             % (what, (lerr > LSE_ATOL).sum(), idx, lse[idx], ref_lse[idx]))
+
+
+def full_check(seqlens, hq, hkv, seed, dev, scale=None, n_outlier=0):
+    x = make_inputs(seqlens, hq, hkv, 128, seed, n_outlier)
+    scale = 128 ** -0.5 if scale is None else scale
+    o, lse = run_gpu(x, hq, hkv, scale, dev)
+    ref_o, ref_lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv, scale)
+    assert_close(o, lse, ref_o, ref_lse, "seqlens=%s hq=%d hkv=%d" % (seqlens, hq, hkv))
+
+
+# -------------------------------------------------------------- small, full
+@pytest.mark.parametrize("S", [1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 255, 256, 257, 1000])
+def test_single_sequence_sweep(dev, S):
+    full_check((S,), 64, 8, 500 + S, dev)
+
+
+def test_varlen_with_empty_and_unit_sequences(dev):
+    full_check((5, 0, 129, 1, 1, 300, 0, 64), 64, 8, 77, dev)
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 2), (128, 1), (64, 4), (64, 32), (8, 4)])
+def test_group_sizes(dev, hq, hkv):
+    full_check((200, 37), hq, hkv, 900 + hq + hkv, dev)
+
+
+def test_workload_s512_full(dev):
+    w = WORKLOADS["s512"]
+    full_check(w.seqlens, w.n_q_heads, w.n_kv_heads, w.seed, dev)
+
+
+def test_uniform_attention_prefix_mean(dev):
+    """q = 0 makes every visible logit 0: o is the running mean of v and
+    lse = ln(i+1). This isolates the P.V path from the Q.K^T path."""
+    x = make_inputs((300,), 64, 8, 128, seed=3)
+    x["q"] = torch.zeros_like(x["q"])
+    o, lse = run_gpu(x, 64, 8, 128 ** -0.5, dev)
+    ref_o, ref_lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], 64, 8, 128 ** -0.5)
+    np.testing.assert_allclose(ref_lse[0], np.log(np.arange(1, 301)), atol=1e-12)
+    assert_close(o, lse, ref_o, ref_lse, "uniform")
+
+
+def test_large_scale_and_outliers_small(dev):
+    full_check((700,), 64, 8, 31, dev, scale=0.5)
+    full_check((700,), 64, 8, 32, dev, n_outlier=4)
+
+
+def test_deterministic_and_stream(dev):
+    x = make_inputs((1000, 333), 64, 8, 128, seed=8)
+    o1, l1 = run_gpu(x, 64, 8, 128 ** -0.5, dev)
+    s = torch.cuda.Stream(dev)
+    o2, l2 = run_gpu(x, 64, 8, 128 ** -0.5, dev, stream=s)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ------------------------------------------------------ full size, sampled
+def sample_rows(cu, hq, n_random, seed):
+    rows = set()
+    T = int(cu[-1])
+    for b in range(len(cu) - 1):
+        s, e = int(cu[b]), int(cu[b + 1])
+        if s == e:
+            continue
+        toks = {s, s + 1, e - 1, e - 2}
+        for edge in range(s + 128, e, 128):
+            toks.update((edge - 1, edge))
+        for t in toks:
+            if s <= t < e:
+                rows.add((int(t) % hq, int(t)))   # rotate heads along tokens
+    rng = np.random.default_rng(seed)
+    for _ in range(n_random):
+        rows.add((int(rng.integers(hq)), int(rng.integers(T))))
+    # every head at the last token of the longest sequence
+    lens = np.diff(np.asarray(cu))
+    b = int(np.argmax(lens))
+    rows.update((h, int(cu[b + 1]) - 1) for h in range(hq))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["s7700", "s10231", "varlen4", "s32768_outlier"])
+def test_full_size_workloads_sampled(dev, name):
+    w = WORKLOADS[name]
+    x = make_workload_inputs(w)
+    o, lse = run_gpu(x, w.n_q_heads, w.n_kv_heads, w.scale, dev)
+    cu = x["cu_seqlens"].numpy()
+    rows = sample_rows(cu, w.n_q_heads, 512, w.seed)
+    ref_o, ref_lse = orc.causal_gqa_rows(x["q"], x["k"], x["v"], cu, w.n_q_heads,
+                                         w.n_kv_heads, w.scale, rows)
+    got_o = o[rows[:, 0], rows[:, 1]]
+    got_l = lse[rows[:, 0], rows[:, 1]]
+    assert_close(got_o, got_l, ref_o, ref_lse, name)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    # every LSE is at least the log of one term and at most log(#keys) above the max
+    assert (lse > -1e4).all()
