@@ -406,12 +406,11 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 ++s_phase;
                 tc_fence_after_sync();
                 float s[kKeys];
+                {
+                    uint32_t sr[kKeys];
+                    tmem_ld128_wait(tS, sr);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t rr[32];
-                    tmem_ld32_wait(tS + (uint32_t)ch * 32u, rr);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(rr[i]);
+                    for (int i = 0; i < kKeys; ++i) s[i] = __uint_as_float(sr[i]);
                 }
                 if (j == n_kv - 1) {
                     // diagonal tile: key (j*128 + i) is visible iff it is <= tok
@@ -420,15 +419,16 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     for (int i = 0; i < kKeys; ++i)
                         if (i > lim) s[i] = -INFINITY;
                 }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                // row max: four running maxima over s[a + 4k], k = 0..31
+                float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                for (int i = 4; i < kKeys; i += 4) {
-                    mx0 = fmaxf(mx0, s[i]);
-                    mx1 = fmaxf(mx1, s[i + 1]);
-                    mx2 = fmaxf(mx2, s[i + 2]);
-                    mx3 = fmaxf(mx3, s[i + 3]);
+                for (int k = 1; k + 1 < kKeys / 4; k += 2) {
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) mx[a] = max3(mx[a], s[4 * k + a], s[4 * k + 4 + a]);
                 }
-                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+#pragma unroll
+                for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], s[kKeys - 4 + a]);
+                const float m_tile = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * c;
                 const float m_new = fmaxf(m, m_tile);
                 float m_use = m, alpha = 1.f;
                 bool rescale = false;
@@ -439,20 +439,23 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     alpha = ex2_approx(m - m_new);
                     rescale = true;
                 }
-                float sum0 = 0.f, sum1 = 0.f;
+                // p = 2^(s*c - m_use), two lanes at a time on the packed FMA
+                // path; the fp32 p feed the row sum, their bf16 rounding is P.
+                const float2 c2 = make_float2(c, c);
+                const float2 nm2 = make_float2(-m_use, -m_use);
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
                 uint32_t pk[kKeys / 2];
 #pragma unroll
                 for (int i = 0; i < kKeys / 2; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[2 * i], c, -m_use));
-                    const float p1 = ex2_approx(fmaf(s[2 * i + 1], c, -m_use));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[i] = pack_bf16x2(p0, p1);
+                    const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2, nm2);
+                    const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    if (i & 1) acc1 = __fadd2_rn(acc1, e); else acc0 = __fadd2_rn(acc0, e);
+                    pk[i] = pack_bf16x2(e.x, e.y);
+                    if ((i & 15) == 15) tmem_st16(tS + (uint32_t)(i - 15), &pk[i - 15]);
                 }
-                l = l * alpha + (sum0 + sum1);
+                const float2 acc = __fadd2_rn(acc0, acc1);
+                l = l * alpha + (acc.x + acc.y);
                 m = m_use;
-                tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-                tmem_st32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
                 if (__any_sync(0xffffffffu, rescale)) {
                     // PV of the previous tile is complete (it was issued
                     // before this S), so O can be scaled in place.

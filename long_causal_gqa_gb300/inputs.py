@@ -10,15 +10,20 @@ tokens; the failing lengths 8184, 8199, 8510 and 10231 are from its
 "Systematic single-variable experiments" table). There is no dataset or
 checkpoint; the values are i.i.d. normal.
 
-Recipe: fp32 `torch.randn` on the CPU from `torch.Generator().manual_seed(seed)`,
-drawn in the order q [Hq,T,D], k [Hkv,T,D], v [Hkv,T,D]; for the outlier
-workload, then `torch.randperm(D)[:n_outlier]` from the same generator picks
-channels that are multiplied by 8 in q and k (all heads, all rows); finally
-each tensor is rounded to bf16 (round to nearest even).
+Recipe: numpy's PCG64 generator, `np.random.default_rng(seed)`, for the
+outlier workload first `rng.permutation(D)[:n_outlier]` picks the channels
+that are multiplied by 8 in q and k (all heads, all rows); then float64
+standard normals are drawn in the order q [Hq,T,D], k [Hkv,T,D], v [Hkv,T,D]
+(in slabs of rows; the stream is the same as one large draw); each value is
+rounded to fp32 and to bf16 (round to nearest even). numpy's generator gives
+the same stream on x86 and aarch64, so a given seed means the same bits on
+every machine (torch's CPU randn does not: its vectorised math differs
+between architectures in the last bit of a few values).
 """
 from dataclasses import dataclass
 from typing import Optional, Tuple
 
+import numpy as np
 import torch
 
 
@@ -75,30 +80,41 @@ def cu_seqlens_of(seqlens) -> torch.Tensor:
     return torch.tensor(cu, dtype=torch.int32)
 
 
+def _normal_bf16(rng, shape, scale_channels=None, std=1.0):
+    """Draws float64 normals row-slab by row-slab (bounded host memory) and
+    returns the bf16 tensor. Channel scaling (x8) happens in fp32 before the
+    bf16 rounding."""
+    out = torch.empty(shape, dtype=torch.bfloat16)
+    flat = out.view(-1, shape[-1])
+    rows = flat.shape[0]
+    step = max(1, (1 << 22) // shape[-1])
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        a = rng.standard_normal((r1 - r0, shape[-1])).astype(np.float32)
+        if std != 1.0:
+            a *= np.float32(std)
+        if scale_channels is not None:
+            a[:, scale_channels] *= np.float32(8.0)
+        flat[r0:r1] = torch.from_numpy(a).to(torch.bfloat16)
+    return out
+
+
 def make_inputs(seqlens, n_q_heads: int, n_kv_heads: int, head_dim: int,
                 seed: int, n_outlier: int = 0, std: float = 1.0):
     """Returns dict(q, k, v: bf16 CPU tensors; cu_seqlens: int32 CPU tensor;
     outlier_channels: the scaled channel indices, or None)."""
     T = sum(int(s) for s in seqlens)
-    g = torch.Generator().manual_seed(int(seed))
-    q = torch.randn((n_q_heads, T, head_dim), generator=g, dtype=torch.float32)
-    k = torch.randn((n_kv_heads, T, head_dim), generator=g, dtype=torch.float32)
-    v = torch.randn((n_kv_heads, T, head_dim), generator=g, dtype=torch.float32)
-    if std != 1.0:
-        q.mul_(std)
-        k.mul_(std)
-        v.mul_(std)
-    idx: Optional[torch.Tensor] = None
-    if n_outlier:
-        idx = torch.randperm(head_dim, generator=g)[:n_outlier]
-        q[:, :, idx] *= 8.0
-        k[:, :, idx] *= 8.0
+    rng = np.random.default_rng(int(seed))
+    idx = rng.permutation(head_dim)[:n_outlier] if n_outlier else None
+    q = _normal_bf16(rng, (n_q_heads, T, head_dim), idx, std)
+    k = _normal_bf16(rng, (n_kv_heads, T, head_dim), idx, std)
+    v = _normal_bf16(rng, (n_kv_heads, T, head_dim), None, std)
     return {
-        "q": q.to(torch.bfloat16),
-        "k": k.to(torch.bfloat16),
-        "v": v.to(torch.bfloat16),
+        "q": q,
+        "k": k,
+        "v": v,
         "cu_seqlens": cu_seqlens_of(seqlens),
-        "outlier_channels": idx,
+        "outlier_channels": None if idx is None else torch.from_numpy(np.asarray(idx)),
     }
 
 
