@@ -16,11 +16,12 @@
 // (256/G consecutive tokens) plus every 128-key tile at or before its last
 // token, so each K/V tile staged in shared memory feeds all G query heads.
 //
-// CTA roles (320 threads, one CTA per SM, persistent over units):
+// CTA roles (352 threads, one CTA per SM, persistent over units):
 //   warps 0-3  softmax for query tile 0 (thread = MMA row = TMEM lane)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer (one lane)
-//   warp  9    TMEM allocator and MMA issuer (one lane)
+//   warp  9    TMEM allocator; MMA issuer for query tile 0 (one lane)
+//   warp 10    MMA issuer for query tile 1 (one lane)
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
 // P (bf16, two per column) overwrites the first 64 columns of its S.
 #pragma once
@@ -35,7 +36,7 @@ constexpr int kRows = 128;                 // MMA M: query rows per tile
 constexpr int kKeys = 128;                 // keys per K/V tile
 constexpr int kStages = 4;                 // K/V ring depth (K and V take one stage each)
 constexpr int kMaxSeqs = 1024;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kSubTileBytes = 128 * 128;          // 128 rows x 64 bf16 (one 128-B swizzle span)
@@ -46,8 +47,8 @@ constexpr uint32_t kBarOff = kKvOff + kStages * kTileBytes;
 // barrier slots
 constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + kStages,
               kBarSFull = 2 + 2 * kStages, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2,
-              kBarDrain = kBarOFull + 2, kNumBars = kBarDrain + 1;
-constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag
+              kBarDrain = kBarOFull + 2, kNumBars = kBarDrain + 2;
+constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag, [2..3] MMA turn counters
 constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if the max grew by > 2^8
@@ -222,10 +223,10 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQFull), 1);
-        mbar_init(bar(kBarQEmpty), 1);
+        mbar_init(bar(kBarQEmpty), 2);              // one commit per MMA issuer
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarKvFull + s), 1);
-            mbar_init(bar(kBarKvEmpty + s), 1);
+            mbar_init(bar(kBarKvEmpty + s), 2);     // one commit per MMA issuer
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(kBarSFull + t), 1);
@@ -233,7 +234,10 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             mbar_init(bar(kBarOFull + t), 1);
         }
         mbar_init(bar(kBarDrain), 1);
+        mbar_init(bar(kBarDrain + 1), 1);
         *abort_flag = 0;
+        misc[2] = 0;
+        misc[3] = 0;
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -297,74 +301,105 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             }
         }
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------- MMA issuer
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // ------------------------------------------------------ MMA issuers
+        // One issuing lane per query tile. tcgen05.mma issue stalls while the
+        // tensor pipe's queue is full, so a single issuer would leave the
+        // pipe idle during its own barrier waits and commits. The two
+        // issuers pass a turn token back and forth (tile 0, tile 1, tile 0,
+        // ...): the tensor pipe alternates between the tiles (so one tile's
+        // softmax overlaps the other tile's MMAs), and each issuer does its
+        // bookkeeping while the other one's batch runs.
         if (lane == 0) {
+            const int t = warp - kMmaWarp;
             constexpr uint32_t idS = idesc_bf16_f32(kRows, kKeys, false);
             constexpr uint32_t idPV = idesc_bf16_f32(kRows, kHeadDim, true);
+            const uint32_t tS = tmem + (uint32_t)t * 128u;
+            const uint32_t tO = tmem + 256u + (uint32_t)t * 128u;
+            const uint32_t sQt = sQ + (uint32_t)t * kTileBytes;
             UnitWalker w;
             w.init(p);
-            uint32_t kv_it = 0, unit_it = 0;
-            uint32_t p_phase[2] = {0, 0};
+            uint32_t kv_it = 0, unit_it = 0, p_phase = 0, turns = 0;
             bool ok = true;
+            // Turn k of issuer 0 follows turn k-1 of issuer 1; turn k of
+            // issuer 1 follows turn k of issuer 0.
+            // The token is a pair of shared-memory counters (a plain volatile
+            // spin wakes faster than an mbarrier): issuer t may start its
+            // turn k once the other issuer has published `done` >= the
+            // count it needs.
+            volatile uint32_t *my_flag = misc + 2 + t;          // written by the other issuer
+            volatile uint32_t *their_flag = misc + 2 + (t ^ 1);
+            auto take_turn = [&]() -> bool {
+                const uint32_t need = t == 0 ? turns : turns + 1;   // other's completed turns
+                if (need == 0) return true;
+                if (*my_flag >= need) return true;
+                const uint64_t t0 = global_timer_ns();
+                for (uint32_t n = 0; *my_flag < need; ++n) {
+                    if ((n & 255u) == 255u) {
+                        if (*abort_flag) return false;
+                        if (global_timer_ns() - t0 > kWaitNs) {
+                            *abort_flag = 1;
+                            atomicOr(&g_timeout_flags, 2u);
+                            return false;
+                        }
+                    }
+                }
+                return true;
+            };
+            auto pass_turn = [&]() {
+                ++turns;
+                *their_flag = turns;
+            };
 
-            auto issue_s = [&](int t, uint32_t stage) {
-                const uint32_t a0 = sQ + (uint32_t)t * kTileBytes;
+            auto issue_s = [&](uint32_t stage) {
                 const uint32_t b0 = sKV + stage * kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * kSubTileBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_bf16_ss(tmem + (uint32_t)t * 128u, kmajor_desc(a0 + off), kmajor_desc(b0 + off),
-                                idS, kk > 0 ? 1u : 0u);
+                    mma_bf16_ss(tS, kmajor_desc(sQt + off), kmajor_desc(b0 + off), idS, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int t, uint32_t stage, bool accumulate) {
+            auto issue_pv = [&](uint32_t stage, bool accumulate) {
                 const uint32_t b0 = sKV + stage * kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    mma_bf16_ts(tmem + 256u + (uint32_t)t * 128u, tmem + (uint32_t)t * 128u + (uint32_t)kk * 8u,
-                                vmn_desc(b0 + (uint32_t)kk * 2048u), idPV,
+                for (int kk = 0; kk < kKeys / 16; ++kk)
+                    mma_bf16_ts(tO, tS + (uint32_t)kk * 8u, vmn_desc(b0 + (uint32_t)kk * 2048u), idPV,
                                 (accumulate || kk > 0) ? 1u : 0u);
-                }
             };
+            const unsigned who = 2u;
 
             for (long long r = 0; ok; ++r) {
                 const long long u = unit_of_round(r);
                 if (u >= p.n_units) break;
                 const Unit un = w.seek(p, u);
                 const int n_kv = (un.block * p.unit_tokens) / kKeys + 1;
-                if (!wait_poll(bar(kBarQFull), unit_it & 1, abort_flag, 2u)) { ok = false; break; }
+                if (!wait_poll(bar(kBarQFull), unit_it & 1, abort_flag, who)) { ok = false; break; }
                 {
                     const uint32_t s = kv_it % kStages;
-                    if (!wait_poll(bar(kBarKvFull + s), (kv_it / kStages) & 1, abort_flag, 2u)) { ok = false; break; }
+                    if (!wait_poll(bar(kBarKvFull + s), (kv_it / kStages) & 1, abort_flag, who)) { ok = false; break; }
+                    if (!take_turn()) { ok = false; break; }
                     tc_fence_after_sync();
-                    issue_s(0, s);
-                    mma_commit(bar(kBarSFull + 0));
-                    issue_s(1, s);
-                    mma_commit(bar(kBarSFull + 1));
+                    issue_s(s);
+                    pass_turn();
+                    mma_commit(bar(kBarSFull + t));
                     mma_commit(bar(kBarKvEmpty + s));
                 }
-                for (int j = 0; j < n_kv && ok; ++j) {
+                for (int j = 0; j < n_kv; ++j) {
                     const uint32_t itv = kv_it + 2u * j + 1u;
                     const uint32_t sv = itv % kStages;
                     const bool more = j + 1 < n_kv;
                     const uint32_t itk = itv + 1u;
                     const uint32_t sk = itk % kStages;
-                    if (!wait_poll(bar(kBarKvFull + sv), (itv / kStages) & 1, abort_flag, 2u)) { ok = false; break; }
-                    if (more && !wait_poll(bar(kBarKvFull + sk), (itk / kStages) & 1, abort_flag, 2u)) { ok = false; break; }
-                    for (int t = 0; t < 2; ++t) {
-                        if (!wait_poll(bar(kBarPFull + t), p_phase[t] & 1, abort_flag, 2u)) { ok = false; break; }
-                        ++p_phase[t];
-                        tc_fence_after_sync();
-                        issue_pv(t, sv, j > 0);
-                        if (more) {
-                            issue_s(t, sk);
-                            mma_commit(bar(kBarSFull + t));
-                        } else {
-                            mma_commit(bar(kBarOFull + t));
-                        }
-                    }
-                    if (!ok) break;
+                    if (!wait_poll(bar(kBarKvFull + sv), (itv / kStages) & 1, abort_flag, who)) { ok = false; break; }
+                    if (more && !wait_poll(bar(kBarKvFull + sk), (itk / kStages) & 1, abort_flag, who)) { ok = false; break; }
+                    if (!wait_poll(bar(kBarPFull + t), p_phase & 1, abort_flag, who)) { ok = false; break; }
+                    ++p_phase;
+                    if (!take_turn()) { ok = false; break; }
+                    tc_fence_after_sync();
+                    issue_pv(sv, j > 0);
+                    if (more) issue_s(sk);
+                    pass_turn();
+                    mma_commit(bar(more ? kBarSFull + t : kBarOFull + t));
                     mma_commit(bar(kBarKvEmpty + sv));
                     if (more) mma_commit(bar(kBarKvEmpty + sk));
                 }
@@ -373,9 +408,9 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 kv_it += 2u * (uint32_t)n_kv;
                 ++unit_it;
             }
-            // Nothing issued may still be running when TMEM is freed.
-            mma_commit(bar(kBarDrain));
-            wait_drain(bar(kBarDrain), 0);
+            // Nothing this lane issued may still be running when TMEM is freed.
+            mma_commit(bar(kBarDrain + t));
+            wait_drain(bar(kBarDrain + t), 0);
         }
         __syncwarp();
     } else {
