@@ -72,6 +72,38 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// Register reallocation between warpgroups (all warps of a warpgroup run
+// the same instruction). The block's total never changes: what one
+// warpgroup gives back is what the others may take.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// Named barrier `id` over `count` threads (whole warps) that also returns
+// the OR of `pred` over all of them, so every participant takes the same
+// decision afterwards.
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // -------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
 {
