@@ -36,6 +36,25 @@ L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def kernel_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    or None when there is none or the kernel sources changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "causal_gqa_fwd_%s.json" % workload)
+    try:
+        with open(path) as f:
+            prof = json.load(f)
+        h = hashlib.sha256()
+        for rel in prof["kernel_source_files"]:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != prof["kernel_source_sha256"]:
+            return None
+        return float(prof["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -265,7 +284,8 @@ def run_ours(args, world, rank, local):
                    "flops_per_step_metric": w.metric_flops(),
                    "flops_per_step_causal_exact": plan.causal_flops},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": kernel_traffic(w.name),
+                     "traffic_unit": "bytes per launch (ncu dram read+write)",
                      "peak_source": "%s bf16_tflops (burst)" % peak_src,
                      "kernel": "h3gqa::causal_gqa_fwd_kernel",
                      "work": "causal FLOPs 2*Hq*D*S*(S+1) per launch"},

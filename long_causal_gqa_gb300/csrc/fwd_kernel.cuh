@@ -191,20 +191,6 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
     return ok;
 }
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr)
-{
-    // K-major operand, 128-B swizzle: 8-row groups 1024 B apart (SBO); the
-    // leading offset is unused for this layout.
-    return sdesc_sw128(saddr, 16, 1024);
-}
-
-__device__ __forceinline__ uint64_t vmn_desc(uint32_t saddr)
-{
-    // V as the MN-major B operand: 64 head dims per 128-B row, the next 64
-    // dims one sub-tile (16 KB) further (LBO), 8-key groups 1024 B apart (SBO).
-    return sdesc_sw128(saddr, kSubTileBytes, 1024);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
 {
@@ -351,20 +337,32 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 *their_flag = turns;
             };
 
+            // Shared-memory descriptors (128-byte swizzle), split in words:
+            // Q and K are K-major (8-row groups 1024 B apart; the leading
+            // offset is unused), V is the MN-major B operand of P.V (64 head
+            // dims per 128-B row, the next 64 dims one 16 KB sub-tile further,
+            // 8-key groups 1024 B apart). A stage or k-step is a constant
+            // added to the low word of stage 0 / of this tile's Q.
+            constexpr uint32_t kHiK = sdesc_hi_sw128(1024);
+            constexpr uint32_t kHiV = sdesc_hi_sw128(1024);
+            const uint32_t q_lo = sdesc_lo(sQt, 16);
+            const uint32_t k_lo0 = sdesc_lo(sKV, 16);
+            const uint32_t v_lo0 = sdesc_lo(sKV, kSubTileBytes);
             auto issue_s = [&](uint32_t stage) {
-                const uint32_t b0 = sKV + stage * kTileBytes;
+                const uint32_t k_lo = k_lo0 + stage * (kTileBytes >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * kSubTileBytes + (uint32_t)(kk & 3) * 32u;
-                    mma_bf16_ss(tS, kmajor_desc(sQt + off), kmajor_desc(b0 + off), idS, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((uint32_t)(kk >> 2) * kSubTileBytes + (uint32_t)(kk & 3) * 32u) >> 4;
+                    mma_bf16_ss(tS, sdesc_make(q_lo + off, kHiK), sdesc_make(k_lo + off, kHiK), idS,
+                                kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](uint32_t stage, bool accumulate) {
-                const uint32_t b0 = sKV + stage * kTileBytes;
+                const uint32_t v_lo = v_lo0 + stage * (kTileBytes >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk)
-                    mma_bf16_ts(tO, tS + (uint32_t)kk * 8u, vmn_desc(b0 + (uint32_t)kk * 2048u), idPV,
-                                (accumulate || kk > 0) ? 1u : 0u);
+                    mma_bf16_ts(tO, tS + (uint32_t)kk * 8u, sdesc_make(v_lo + (uint32_t)kk * (2048u >> 4), kHiV),
+                                idPV, (accumulate || kk > 0) ? 1u : 0u);
             };
             const unsigned who = 2u;
 

@@ -266,6 +266,27 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// The same descriptor split in two 32-bit words: the low word carries the
+// start address and the leading byte offset, the high word the stride byte
+// offset, version and swizzle mode (a per-layout constant). Stepping a
+// descriptor through a tile is then one 32-bit add on the low word (no
+// carry: shared-memory addresses stay below 256 KB, i.e. < 2^14 in 16-byte
+// units).
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes)
+{
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo_bytes)
+{
+    return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+__device__ __forceinline__ uint64_t sdesc_make(uint32_t lo, uint32_t hi)
+{
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
 // 4-5 = 1), bf16 A and B (bits 7-9 and 10-12 = 1), A K-major (bit 15 = 0),
 // B K-major or MN-major (bit 16), N/8 in bits 17-22, M/16 in bits 24-28.
