@@ -152,15 +152,14 @@ __device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, volatil
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    uint32_t n = 0;
+    // Each failed poll has been suspended up to the capped hint (20 us), so
+    // checking the clock and the abort flag on every one costs nothing.
     while (!mbar_try_wait_capped(bar, parity)) {
-        if (((++n) & 31u) == 0) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitNs) {
-                *abort_flag = 1;
-                atomicOr(&g_timeout_flags, who);
-                return false;
-            }
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            atomicOr(&g_timeout_flags, who);
+            return false;
         }
     }
     return true;

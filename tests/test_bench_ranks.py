@@ -1,0 +1,42 @@
+"""Multi-rank host logic of bench.py on CPU (gloo, world size 2): every rank
+times its own replica; the reported time is the slowest rank's and the value
+counts every rank's FLOPs."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    w, r, _ = bench.dist_setup()
+    ms = 1.0 + r                      # rank 1 is the slower one
+    slowest = bench.max_over_ranks(ms, w, torch.device("cpu"))
+    out[rank] = (w, slowest, bench.whole_job_value(10e12, w, slowest))
+    bench.barrier(w)
+    dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_slowest_time():
+    port = _free_port()
+    manager = mp.Manager()
+    out = manager.dict()
+    mp.start_processes(_worker, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
+    assert out[0] == out[1]
+    world, slowest, value = out[0]
+    assert world == 2 and slowest == 2.0
+    # 2 ranks x 10 TFLOP in 2 ms = 10,000 TFLOP/s
+    assert value == pytest.approx(2 * 10e12 / 2e-3 / 1e12)
