@@ -31,6 +31,16 @@ from long_causal_gqa_gb300 import binding  # noqa: E402
 from long_causal_gqa_gb300.inputs import HEADLINE, WORKLOADS, make_workload_inputs  # noqa: E402
 
 METRIC = "causal GQA prefill TFLOP/s at S=10231 (Hq64/Hkv8/D128), % of BF16 peak"
+EPILOGUES = {"bf16_head": (False, False), "bf16_token": (True, False), "int8_token": (True, True),
+             "int8_head": (False, True)}
+
+
+def metric_name(w, epilogue):
+    if w.name == HEADLINE and epilogue == "bf16_head":
+        return METRIC
+    kind = "causal GQA prefill" if w.causal else "bidirectional GQA attention"
+    return "%s TFLOP/s, workload %s (Hq%d/Hkv%d/D%d), output %s" % (
+        kind, w.name, w.n_q_heads, w.n_kv_heads, w.head_dim, epilogue)
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -153,18 +163,24 @@ def oracle_sample_rate(x, w, seconds, seed):
     rng = np.random.default_rng(seed)
     T = int(cu[-1])
 
+    ends = np.repeat(cu[1:], np.diff(cu))
+
     def run(n):
         rows = np.stack([rng.integers(0, w.n_q_heads, n), rng.integers(0, T, n)], axis=1)
-        keys = rows[:, 1] - starts[rows[:, 1]] + 1
+        if w.causal:
+            keys = rows[:, 1] - starts[rows[:, 1]] + 1
+        else:
+            keys = ends[rows[:, 1]] - starts[rows[:, 1]]
         t0 = time.perf_counter()
-        orc.causal_gqa_rows(x["q"], x["k"], x["v"], cu, w.n_q_heads, w.n_kv_heads, w.scale, rows)
+        orc.causal_gqa_rows(x["q"], x["k"], x["v"], cu, w.n_q_heads, w.n_kv_heads, w.scale, rows,
+                            causal=w.causal)
         dt = time.perf_counter() - t0
         return float(keys.sum()) * 4 * w.head_dim, dt
 
     flops, dt = run(64)                      # calibration
     n = int(max(64, min(2_000_000, 64 * seconds / max(dt, 1e-3))))
     flops, dt = run(n)
-    desc = ("%d random (head, query row) pairs of %s, each row's full causal attention in fp64; "
+    desc = ("%d random (head, query row) pairs of %s, each row's full attention in fp64; "
             "FLOPs counted as 4*D per visible (query, key) pair" % (n, w.name))
     return flops / dt / 1e12, desc, orc.max_threads(), n
 
@@ -184,7 +200,7 @@ def run_reference(args, world, rank):
             rates.append(r)
     value = float(np.mean(rates))
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": metric_name(w, args.epilogue), "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": w.metric_flops() / (value * 1e12) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -203,20 +219,33 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     binding.load()
     w = WORKLOADS[args.workload]
+    token_major, out_int8 = EPILOGUES[args.epilogue]
     x = make_workload_inputs(w)
     cu = x["cu_seqlens"]
-    plan = binding.h3gqa_make_plan(cu, w.n_q_heads, w.n_kv_heads, w.head_dim)
+    plan = binding.h3gqa_attention_plan(cu, w.n_q_heads, w.n_kv_heads, w.head_dim, w.causal)
     stream = torch.cuda.Stream(device)
     q, k, v = (x[n].to(device) for n in ("q", "k", "v"))
-    o = torch.empty_like(q)
+    oshape = (w.total_tokens, w.n_q_heads, w.head_dim) if token_major else tuple(q.shape)
+    o = torch.empty(oshape, dtype=torch.int8 if out_int8 else torch.bfloat16, device=device)
+    o_scale = (torch.empty(oshape[:2], dtype=torch.float32, device=device) if out_int8
+               else None)
     lse = torch.empty((w.n_q_heads, w.total_tokens), dtype=torch.float32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     sh = stream.cuda_stream
+    default_call = w.causal and args.epilogue == "bf16_head"
+    opts = binding.make_options(w.causal, binding.H3GQA_LAYOUT_TOKEN_MAJOR if token_major
+                                else binding.H3GQA_LAYOUT_HEAD_MAJOR, out_int8,
+                                o_scale.data_ptr() if o_scale is not None else None)
 
     def launch():
-        binding.h3gqa_causal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                 lse.data_ptr(), cu, w.n_q_heads, w.n_kv_heads, w.head_dim,
-                                 w.scale, sh)
+        if default_call:
+            binding.h3gqa_causal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), cu, w.n_q_heads, w.n_kv_heads,
+                                     w.head_dim, w.scale, sh)
+        else:
+            binding.h3gqa_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), cu, w.n_q_heads, w.n_kv_heads,
+                                        w.head_dim, w.scale, opts, sh)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -251,8 +280,11 @@ def run_ours(args, world, rank, local):
     qh, kh, vh = (x[n].pin_memory() for n in ("q", "k", "v"))
     oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    sch = (torch.empty(o_scale.shape, dtype=o_scale.dtype, pin_memory=True)
+           if o_scale is not None else None)
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size() + \
+        (sch.numel() * sch.element_size() if sch is not None else 0)
     e2e_steps = max(3, min(args.steps, 20))
     with torch.cuda.stream(stream):
         for i in range(e2e_steps + 2):
@@ -265,6 +297,8 @@ def run_ours(args, world, rank, local):
             launch()
             oh.copy_(o, non_blocking=True)
             lh.copy_(lse, non_blocking=True)
+            if sch is not None:
+                sch.copy_(o_scale, non_blocking=True)
             stream.synchronize()
     e2e_ms = (time.perf_counter() - te0) * 1e3 / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world, device)
@@ -277,23 +311,25 @@ def run_ours(args, world, rank, local):
     value = whole_job_value(w.metric_flops(), world, ms_max)
     achieved = plan.causal_flops / (ms * 1e-3) / 1e12
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": metric_name(w, args.epilogue), "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q/k/v; no dataset)",
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "config": {"workload": w.name, "seqlens": list(w.seqlens), "n_q_heads": w.n_q_heads,
-                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
+                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "causal": w.causal,
+                   "output": args.epilogue,
                    "scale": w.scale, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed before every step (256 MB write, outside the kernel events)",
                    "flops_per_step_metric": w.metric_flops(),
                    "flops_per_step_causal_exact": plan.causal_flops},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": kernel_traffic(w.name),
+                     "frac": achieved / peak,
+                     "traffic": kernel_traffic(w.name) if args.epilogue == "bf16_head" else None,
                      "traffic_unit": "bytes per launch (ncu dram read+write)",
                      "peak_source": "%s bf16_tflops (burst)" % peak_src,
                      "kernel": "h3gqa::causal_gqa_fwd_kernel",
-                     "work": "causal FLOPs 2*Hq*D*S*(S+1) per launch"},
+                     "work": "4*D FLOPs per visible (query, key, head) pair per launch"},
         "e2e": {"value": whole_job_value(w.metric_flops(), world, e2e_ms), "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
@@ -314,6 +350,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
+    ap.add_argument("--epilogue", choices=sorted(EPILOGUES), default="bf16_head",
+                    help="output form: bf16 or int8 codes (+ per-row scales), head- or token-major")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -84,6 +84,55 @@ h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v,
                               int n_q_heads, int n_kv_heads, int head_dim,
                               float scale, h3gqa_stream_t stream);
 
+/*
+ * Options of h3gqa_attention_fwd: the bidirectional variant and the output
+ * forms the out-projection consumes.
+ *
+ * causal = 0 is the same attention without the causal rule (every query of a
+ * sequence sees every key of that sequence): the long bidirectional
+ * attention of H3's DiT, whose 19316- and 34121-row forwards appear in
+ * tgo-app-dev/vpipe issue #10, and which the h3.c README ("Metal 4 and
+ * TensorOps paths") keeps on MPSGraph at those sizes.
+ *
+ * out_layout = H3GQA_LAYOUT_TOKEN_MAJOR writes o as [T][Hq][head_dim], the
+ * row-major order the out-projection reads, instead of leaving it in
+ * [head,row,dimension] order for a separate gather (h3.c README, "Profiling
+ * and diagnostic paths", which gathers and int8-quantizes the SDPA output on
+ * its way into the out-projection).
+ *
+ * out_int8 = 1 writes o as int8 codes with one fp32 scale per (token, head)
+ * row of head_dim values: scale = max|o_row| / 127 (1 for an all-zero row),
+ * code = round-to-nearest-even(o / scale) clamped to [-127, 127], so
+ * o ~= code * scale. o then holds 1 byte per element (16-byte aligned) and
+ * o_scale is laid out like o without the last dimension.
+ */
+typedef enum {
+    H3GQA_LAYOUT_HEAD_MAJOR = 0,     /* [Hq][T][head_dim] */
+    H3GQA_LAYOUT_TOKEN_MAJOR = 1     /* [T][Hq][head_dim] */
+} h3gqa_layout;
+
+typedef struct {
+    int32_t causal;        /* 1: key j visible to query i iff j <= i; 0: every key of the sequence */
+    int32_t out_layout;    /* h3gqa_layout of o (and of o_scale) */
+    int32_t out_int8;      /* 0: o is bf16; 1: o is int8 codes plus o_scale */
+    int32_t reserved;      /* must be 0 */
+    float *o_scale;        /* device fp32 [Hq][T] or [T][Hq], 4-byte aligned; required iff out_int8 */
+} h3gqa_options;
+
+/*
+ * h3gqa_causal_fwd with options (NULL options = causal, head-major bf16 o,
+ * i.e. exactly h3gqa_causal_fwd). Arguments and errors as for
+ * h3gqa_causal_fwd; in addition an options value outside the ranges above,
+ * or out_int8 without a valid o_scale, returns H3GQA_ERR_INVALID_ARG. lse is
+ * always [Hq][T].
+ */
+h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v,
+                                 void *o, float *lse,
+                                 const int32_t *cu_seqlens, int n_seqs,
+                                 int n_q_heads, int n_kv_heads, int head_dim,
+                                 float scale, const h3gqa_options *options,
+                                 h3gqa_stream_t stream);
+
 /* Work plan of one h3gqa_causal_fwd call, computed on the host only (no GPU
  * needed). A unit is (sequence, block of 256/G tokens, KV head); it owns two
  * 128-row query tiles (G heads x 128/G tokens each) and visits every 128-key
@@ -93,9 +142,9 @@ typedef struct {
     int64_t n_units;            /* work units */
     int64_t n_kv_tiles;         /* sum over units of 128-key tiles visited */
     double tensor_flops;        /* FLOPs the MMAs execute: n_kv_tiles * 2 tiles * 2 GEMMs * 2*128^3 */
-    double causal_flops;        /* needed FLOPs: sum_b 2*Hq*D*S_b*(S_b+1) */
-    double metric_flops;        /* headline count: sum_b 2*Hq*D*S_b^2 */
-    double exp2_count;          /* needed exponentials: sum_b Hq*S_b*(S_b+1)/2 */
+    double causal_flops;        /* needed FLOPs, 4*D per visible (query, key, head): causal sum_b 2*Hq*D*S_b*(S_b+1) */
+    double metric_flops;        /* headline count: causal sum_b 2*Hq*D*S_b^2 */
+    double exp2_count;          /* needed exponentials, one per visible pair: causal sum_b Hq*S_b*(S_b+1)/2 */
     double algorithmic_bytes;   /* q,k,v read once + o,lse written once */
     int32_t tokens_per_unit;    /* 256 / G */
     int32_t max_kv_tiles;       /* most 128-key tiles any unit visits */
@@ -107,6 +156,13 @@ typedef struct {
 h3gqa_status h3gqa_make_plan(const int32_t *cu_seqlens, int n_seqs,
                              int n_q_heads, int n_kv_heads, int head_dim,
                              h3gqa_plan *plan);
+
+/* The plan of h3gqa_attention_fwd with the given causal flag. For causal = 0
+ * every unit visits all key tiles of its sequence, causal_flops counts all
+ * (query, key) pairs (4*Hq*D*S^2) and metric_flops equals it. */
+h3gqa_status h3gqa_attention_plan(const int32_t *cu_seqlens, int n_seqs,
+                                  int n_q_heads, int n_kv_heads, int head_dim,
+                                  int32_t causal, h3gqa_plan *plan);
 
 /* Waits for `stream`, then reads and clears the current device's timeout
  * flag. Returns H3GQA_ERR_TIMEOUT if any kernel of this library on this

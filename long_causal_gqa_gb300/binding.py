@@ -18,8 +18,12 @@ H3GQA_ERR_ARCH = 3
 H3GQA_ERR_CUDA = 4
 H3GQA_ERR_TIMEOUT = 5
 
-EXPORTED = ("h3gqa_causal_fwd", "h3gqa_make_plan", "h3gqa_sync_and_check",
-            "h3gqa_status_string", "h3gqa_version")
+EXPORTED = ("h3gqa_causal_fwd", "h3gqa_attention_fwd", "h3gqa_make_plan",
+            "h3gqa_attention_plan", "h3gqa_sync_and_check", "h3gqa_status_string",
+            "h3gqa_version")
+
+H3GQA_LAYOUT_HEAD_MAJOR = 0
+H3GQA_LAYOUT_TOKEN_MAJOR = 1
 
 
 class H3GQAError(RuntimeError):
@@ -44,6 +48,16 @@ class h3gqa_plan(ctypes.Structure):
     ]
 
 
+class h3gqa_options(ctypes.Structure):
+    _fields_ = [
+        ("causal", ctypes.c_int32),
+        ("out_layout", ctypes.c_int32),
+        ("out_int8", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("o_scale", ctypes.c_void_p),
+    ]
+
+
 _LIB = None
 
 
@@ -60,9 +74,16 @@ def load(path: str = LIB_PATH):
     lib.h3gqa_causal_fwd.argtypes = [vp, vp, vp, vp, vp, i32p, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_float, vp]
     lib.h3gqa_causal_fwd.restype = ctypes.c_int
+    lib.h3gqa_attention_fwd.argtypes = [vp, vp, vp, vp, vp, i32p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                        ctypes.POINTER(h3gqa_options), vp]
+    lib.h3gqa_attention_fwd.restype = ctypes.c_int
     lib.h3gqa_make_plan.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.POINTER(h3gqa_plan)]
     lib.h3gqa_make_plan.restype = ctypes.c_int
+    lib.h3gqa_attention_plan.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int32, ctypes.POINTER(h3gqa_plan)]
+    lib.h3gqa_attention_plan.restype = ctypes.c_int
     lib.h3gqa_sync_and_check.argtypes = [vp]
     lib.h3gqa_sync_and_check.restype = ctypes.c_int
     lib.h3gqa_status_string.argtypes = [ctypes.c_int]
@@ -99,6 +120,36 @@ def h3gqa_make_plan(cu_seqlens, n_q_heads, n_kv_heads, head_dim=128):
     return plan
 
 
+def h3gqa_attention_plan(cu_seqlens, n_q_heads, n_kv_heads, head_dim=128, causal=True):
+    """Host-only work plan of h3gqa_attention_fwd for the causal flag."""
+    arr, n = _cu_array(cu_seqlens)
+    plan = h3gqa_plan()
+    st = load().h3gqa_attention_plan(arr, n, int(n_q_heads), int(n_kv_heads), int(head_dim),
+                                     1 if causal else 0, ctypes.byref(plan))
+    if st != H3GQA_OK:
+        raise H3GQAError(st, "h3gqa_attention_plan")
+    return plan
+
+
+def make_options(causal=True, out_layout=H3GQA_LAYOUT_HEAD_MAJOR, out_int8=False,
+                 o_scale_ptr=None, reserved=0):
+    return h3gqa_options(1 if causal else 0, int(out_layout), 1 if out_int8 else 0,
+                         int(reserved), o_scale_ptr or None)
+
+
+def h3gqa_attention_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, cu_seqlens, n_q_heads, n_kv_heads,
+                        head_dim, scale, options=None, stream=0, check=True):
+    """Raw call with an h3gqa_options (or None for the causal defaults)."""
+    arr, n = _cu_array(cu_seqlens)
+    st = load().h3gqa_attention_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, arr, n, int(n_q_heads),
+                                    int(n_kv_heads), int(head_dim), ctypes.c_float(scale),
+                                    ctypes.byref(options) if options is not None else None,
+                                    stream or None)
+    if check and st != H3GQA_OK:
+        raise H3GQAError(st, "h3gqa_attention_fwd")
+    return st
+
+
 def h3gqa_causal_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, cu_seqlens, n_q_heads, n_kv_heads,
                      head_dim, scale, stream=0, check=True):
     """Raw call: device pointers as ints, cu_seqlens host-side, stream handle as int.
@@ -117,6 +168,37 @@ def h3gqa_sync_and_check(stream=0, check=True):
     if check and st != H3GQA_OK:
         raise H3GQAError(st, "h3gqa_sync_and_check")
     return st
+
+
+def attention_fwd(q, k, v, cu_seqlens, scale=None, causal=True, token_major=False,
+                  out_int8=False, stream=None):
+    """Torch front end of h3gqa_attention_fwd. Returns (o, lse, o_scale):
+    o bf16 (or int8 codes) in [Hq,T,D] or [T,Hq,D] order, lse fp32 [Hq,T],
+    o_scale fp32 [Hq,T] / [T,Hq] for int8 output (else None)."""
+    import torch
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be [heads, T, head_dim]")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bf16 CUDA tensor" % name)
+    hq, T, d = q.shape
+    hkv = k.shape[0]
+    if scale is None:
+        scale = d ** -0.5
+    shape = (T, hq, d) if token_major else (hq, T, d)
+    o = torch.empty(shape, dtype=torch.int8 if out_int8 else torch.bfloat16, device=q.device)
+    lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    o_scale = None
+    if out_int8:
+        o_scale = torch.empty(shape[:2], dtype=torch.float32, device=q.device)
+    opts = make_options(causal, H3GQA_LAYOUT_TOKEN_MAJOR if token_major else
+                        H3GQA_LAYOUT_HEAD_MAJOR, out_int8,
+                        o_scale.data_ptr() if o_scale is not None else None)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    h3gqa_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        cu_seqlens, hq, hkv, d, float(scale), opts, stream.cuda_stream)
+    return o, lse, o_scale
 
 
 def causal_gqa_fwd(q, k, v, cu_seqlens, scale=None, o=None, lse=None, stream=None):

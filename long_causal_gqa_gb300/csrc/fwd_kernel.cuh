@@ -66,8 +66,13 @@ struct FwdParams {
     CUtensorMap map_q;      // q [Hq][T][128], box {64, 128/G, G}
     CUtensorMap map_k;      // k [Hkv][T][128], box {64, 128, 1}
     CUtensorMap map_v;      // v [Hkv][T][128], box {64, 128, 1}
-    uint16_t *o;            // bf16 [Hq][T][128]
+    void *o;                // bf16 (or int8 codes) [Hq][T][128] or [T][Hq][128]
     float *lse;             // fp32 [Hq][T]
+    float *o_scale;         // int8 output only: one fp32 scale per (token, head) row
+    int causal;             // 1: key j visible to query i iff j <= i; 0: all keys of the sequence
+    int out_token_major;    // 0: o is [Hq][T][128]; 1: o is [T][Hq][128] (o_scale likewise)
+    int out_int8;           // 0: bf16 o; 1: int8 codes, o ~= code * o_scale
+    int n_q_heads;
     long long total_tokens;
     long long n_units;
     int n_kv_heads;
@@ -114,9 +119,31 @@ struct UnitWalker {
         return hi > lo ? hi - lo : 0;
     }
 
+    __device__ __forceinline__ int blocks_of(const FwdParams &p, int seq) const
+    {
+        return (p.seq_len[seq] + p.unit_tokens - 1) / p.unit_tokens;
+    }
+
     // u must not decrease from one call to the next, and u < n_units.
     __device__ __forceinline__ Unit seek(const FwdParams &p, long long u)
     {
+        if (!p.causal) {
+            // Without the causal rule every unit of a sequence visits all of
+            // its key tiles: longest sequence first, then block, then KV head.
+            for (;;) {
+                const long long cnt = (long long)blocks_of(p, i) * p.n_kv_heads;
+                if (u < base + cnt) break;
+                base += cnt;
+                ++i;
+            }
+            const long long j = u - base;
+            Unit r;
+            r.seq_start = p.seq_start[i];
+            r.seq_len = p.seq_len[i];
+            r.kv_head = (int)(j % p.n_kv_heads);
+            r.block = (int)(j / p.n_kv_heads);
+            return r;
+        }
         for (;;) {
             const long long cnt = (long long)blocks_in_class(p, c, i) * p.n_kv_heads;
             if (u < base + cnt) break;
@@ -136,6 +163,13 @@ struct UnitWalker {
         return r;
     }
 };
+
+// Key tiles a unit visits: up to its last token (causal), or the whole
+// sequence.
+__device__ __forceinline__ int unit_kv_tiles(const FwdParams &p, const Unit &un)
+{
+    return p.causal ? (un.block * p.unit_tokens) / kKeys + 1 : (un.seq_len + kKeys - 1) / kKeys;
+}
 
 // Round r of the static schedule hands CTA x the unit r*grid + x on even
 // rounds and r*grid + (grid-1-x) on odd ones (a snake over the longest-first
@@ -252,7 +286,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 if (u >= p.n_units) break;
                 const Unit un = w.seek(p, u);
                 const int tb = un.block * p.unit_tokens;
-                const int n_kv = tb / kKeys + 1;
+                const int n_kv = unit_kv_tiles(p, un);
                 if (!wait_poll(bar(kBarQEmpty), (unit_it & 1) ^ 1, abort_flag, 1u)) { ok = false; break; }
                 mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
                 last_q_parity = unit_it & 1;
@@ -369,7 +403,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 const long long u = unit_of_round(r);
                 if (u >= p.n_units) break;
                 const Unit un = w.seek(p, u);
-                const int n_kv = (un.block * p.unit_tokens) / kKeys + 1;
+                const int n_kv = unit_kv_tiles(p, un);
                 if (!wait_poll(bar(kBarQFull), unit_it & 1, abort_flag, who)) { ok = false; break; }
                 {
                     const uint32_t s = kv_it % kStages;
@@ -429,7 +463,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             if (u >= p.n_units) break;
             const Unit un = w.seek(p, u);
             const int tb = un.block * p.unit_tokens;
-            const int n_kv = tb / kKeys + 1;
+            const int n_kv = unit_kv_tiles(p, un);
             const int tok = tb + t * p.tile_tokens + tok_in_tile;   // token inside its sequence
             float m = -INFINITY;   // running max of the scaled logits, log2 units
             float l = 0.f;         // running sum of exp2(logit - m)
@@ -445,8 +479,9 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     for (int i = 0; i < kKeys; ++i) s[i] = __uint_as_float(sr[i]);
                 }
                 if (j == n_kv - 1) {
-                    // diagonal tile: key (j*128 + i) is visible iff it is <= tok
-                    const int lim = tok - j * kKeys;
+                    // last tile: key (j*128 + i) is visible iff it is <= tok
+                    // (causal) or inside the sequence (bidirectional)
+                    const int lim = (p.causal ? tok : un.seq_len - 1) - j * kKeys;
 #pragma unroll
                     for (int i = 0; i < kKeys; ++i)
                         if (i > lim) s[i] = -INFINITY;
@@ -511,23 +546,61 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             tc_fence_after_sync();
             const float inv_l = 1.0f / l;
             const bool valid = tok < un.seq_len;
-            const long long grow = (long long)(un.kv_head * p.group + head_in_group) * p.total_tokens +
-                                   un.seq_start + tok;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * kHeadDim);
+            const int head = un.kv_head * p.group + head_in_group;
+            const long long tok_g = (long long)un.seq_start + tok;
+            const long long grow = (long long)head * p.total_tokens + tok_g;          // [Hq][T] index
+            const long long orow = p.out_token_major ? tok_g * p.n_q_heads + head : grow;
+            if (!p.out_int8) {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + orow * kHeadDim);
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t rr[32];
-                tmem_ld32_wait(tO + (uint32_t)ch * 32u, rr);
-                if (valid) {
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t rr[32];
+                    tmem_ld32_wait(tO + (uint32_t)ch * 32u, rr);
+                    if (valid) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 pkt;
-                        pkt.x = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 0]) * inv_l, __uint_as_float(rr[v4 * 8 + 1]) * inv_l);
-                        pkt.y = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 2]) * inv_l, __uint_as_float(rr[v4 * 8 + 3]) * inv_l);
-                        pkt.z = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 4]) * inv_l, __uint_as_float(rr[v4 * 8 + 5]) * inv_l);
-                        pkt.w = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 6]) * inv_l, __uint_as_float(rr[v4 * 8 + 7]) * inv_l);
-                        dst[ch * 4 + v4] = pkt;
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 pkt;
+                            pkt.x = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 0]) * inv_l, __uint_as_float(rr[v4 * 8 + 1]) * inv_l);
+                            pkt.y = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 2]) * inv_l, __uint_as_float(rr[v4 * 8 + 3]) * inv_l);
+                            pkt.z = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 4]) * inv_l, __uint_as_float(rr[v4 * 8 + 5]) * inv_l);
+                            pkt.w = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 6]) * inv_l, __uint_as_float(rr[v4 * 8 + 7]) * inv_l);
+                            dst[ch * 4 + v4] = pkt;
+                        }
                     }
+                }
+            } else {
+                // int8 with one scale per (token, head) row: scale = max|o| / 127,
+                // code = round-to-nearest-even(o / scale), o ~= code * scale.
+                float x[kHeadDim];
+                {
+                    uint32_t rr[kHeadDim];
+                    tmem_ld128_wait(tO, rr);
+#pragma unroll
+                    for (int i = 0; i < kHeadDim; ++i) x[i] = __uint_as_float(rr[i]) * inv_l;
+                }
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < kHeadDim; ++i) amax = fmaxf(amax, fabsf(x[i]));
+                const float qscale = amax > 0.f ? amax / 127.0f : 1.0f;
+                const float inv_q = amax > 0.f ? 127.0f / amax : 0.0f;
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<int8_t *>(p.o) + orow * kHeadDim);
+#pragma unroll
+                    for (int v4 = 0; v4 < kHeadDim / 16; ++v4) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            uint32_t word = 0;
+#pragma unroll
+                            for (int bi = 0; bi < 4; ++bi) {
+                                const int c = __float2int_rn(fminf(fmaxf(x[v4 * 16 + wi * 4 + bi] * inv_q, -127.f), 127.f));
+                                word |= ((uint32_t)c & 0xFFu) << (8 * bi);
+                            }
+                            w4[wi] = word;
+                        }
+                        dst[v4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    p.o_scale[orow] = qscale;
                 }
             }
             if (valid) p.lse[grow] = (m + __log2f(l)) * 0.69314718055994531f;

@@ -44,7 +44,7 @@ int ilog2(int x)
 
 // Shape checks shared by the plan query and the forward call; no CUDA.
 h3gqa_status build_plan(const int32_t *cu, int n_seqs, int hq, int hkv, int head_dim,
-                        HostPlan *out)
+                        bool causal, HostPlan *out)
 {
     if (cu == nullptr || n_seqs < 0) return H3GQA_ERR_INVALID_ARG;
     if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return H3GQA_ERR_INVALID_ARG;
@@ -77,13 +77,18 @@ h3gqa_status build_plan(const int32_t *cu, int n_seqs, int hq, int hkv, int head
         p.len.push_back(len);
         const long long nblk = (len + p.unit_tokens - 1) / p.unit_tokens;
         p.n_units += nblk * hkv;
-        // block k visits floor(k*unit/128) + 1 key tiles
-        for (long long k = 0; k < nblk; ++k)
-            p.n_kv_tiles += (k * p.unit_tokens / h3gqa::kKeys + 1) * hkv;
+        if (causal) {
+            // block k visits floor(k*unit/128) + 1 key tiles
+            for (long long k = 0; k < nblk; ++k)
+                p.n_kv_tiles += (k * p.unit_tokens / h3gqa::kKeys + 1) * hkv;
+        } else {
+            p.n_kv_tiles += nblk * ((len + h3gqa::kKeys - 1) / h3gqa::kKeys) * hkv;
+        }
     }
     if (!p.len.empty()) {
         const long long nblk0 = (p.len[0] + p.unit_tokens - 1) / p.unit_tokens;
-        p.c_max = (int)((nblk0 + p.blocks_per_class - 1) / p.blocks_per_class);
+        p.c_max = causal ? (int)((nblk0 + p.blocks_per_class - 1) / p.blocks_per_class)
+                         : (p.len[0] + h3gqa::kKeys - 1) / h3gqa::kKeys;
     }
     *out = std::move(p);
     return H3GQA_OK;
@@ -170,25 +175,33 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 extern "C" {
 
-h3gqa_status h3gqa_make_plan(const int32_t *cu_seqlens, int n_seqs, int n_q_heads,
-                             int n_kv_heads, int head_dim, h3gqa_plan *plan)
+h3gqa_status h3gqa_attention_plan(const int32_t *cu_seqlens, int n_seqs, int n_q_heads,
+                                  int n_kv_heads, int head_dim, int32_t causal, h3gqa_plan *plan)
 {
-    if (plan == nullptr) return H3GQA_ERR_INVALID_ARG;
+    if (plan == nullptr || (causal != 0 && causal != 1)) return H3GQA_ERR_INVALID_ARG;
     HostPlan hp;
-    const h3gqa_status st = build_plan(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim, &hp);
+    const h3gqa_status st =
+        build_plan(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim, causal != 0, &hp);
     if (st != H3GQA_OK) return st;
     std::memset(plan, 0, sizeof(*plan));
     plan->total_tokens = hp.total_tokens;
     plan->n_units = hp.n_units;
     plan->n_kv_tiles = hp.n_kv_tiles;
     plan->tensor_flops = (double)hp.n_kv_tiles * 2.0 * 2.0 * 2.0 * 128.0 * 128.0 * 128.0;
-    double causal = 0, metric = 0, ex = 0;
-    for (int s : hp.len) {
-        causal += 2.0 * n_q_heads * head_dim * (double)s * (double)(s + 1);
-        metric += 2.0 * n_q_heads * head_dim * (double)s * (double)s;
-        ex += (double)n_q_heads * (double)s * (double)(s + 1) / 2.0;
+    double needed = 0, metric = 0, ex = 0;
+    for (int len : hp.len) {
+        const double S = (double)len;
+        if (causal) {
+            needed += 2.0 * n_q_heads * head_dim * S * (S + 1.0);
+            metric += 2.0 * n_q_heads * head_dim * S * S;
+            ex += (double)n_q_heads * S * (S + 1.0) / 2.0;
+        } else {
+            needed += 4.0 * n_q_heads * head_dim * S * S;
+            metric += 4.0 * n_q_heads * head_dim * S * S;
+            ex += (double)n_q_heads * S * S;
+        }
     }
-    plan->causal_flops = causal;
+    plan->causal_flops = needed;
     plan->metric_flops = metric;
     plan->exp2_count = ex;
     const double T = (double)hp.total_tokens;
@@ -199,17 +212,33 @@ h3gqa_status h3gqa_make_plan(const int32_t *cu_seqlens, int n_seqs, int n_q_head
     return H3GQA_OK;
 }
 
-h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
-                              const int32_t *cu_seqlens, int n_seqs, int n_q_heads,
-                              int n_kv_heads, int head_dim, float scale, h3gqa_stream_t stream)
+h3gqa_status h3gqa_make_plan(const int32_t *cu_seqlens, int n_seqs, int n_q_heads,
+                             int n_kv_heads, int head_dim, h3gqa_plan *plan)
 {
+    return h3gqa_attention_plan(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim, 1, plan);
+}
+
+h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                                 const int32_t *cu_seqlens, int n_seqs, int n_q_heads,
+                                 int n_kv_heads, int head_dim, float scale,
+                                 const h3gqa_options *options, h3gqa_stream_t stream)
+{
+    h3gqa_options opt = {1, H3GQA_LAYOUT_HEAD_MAJOR, 0, 0, nullptr};
+    if (options != nullptr) opt = *options;
+    if ((opt.causal != 0 && opt.causal != 1) || opt.reserved != 0 ||
+        (opt.out_layout != H3GQA_LAYOUT_HEAD_MAJOR && opt.out_layout != H3GQA_LAYOUT_TOKEN_MAJOR) ||
+        (opt.out_int8 != 0 && opt.out_int8 != 1))
+        return H3GQA_ERR_INVALID_ARG;
+    if (opt.out_int8 && (opt.o_scale == nullptr || !aligned(opt.o_scale, 4)))
+        return H3GQA_ERR_INVALID_ARG;
     if (!q || !k || !v || !o || !lse) return H3GQA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
         !aligned(lse, 4))
         return H3GQA_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return H3GQA_ERR_INVALID_ARG;
     HostPlan hp;
-    h3gqa_status st = build_plan(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim, &hp);
+    h3gqa_status st =
+        build_plan(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim, opt.causal != 0, &hp);
     if (st != H3GQA_OK) return st;
     if (hp.n_units == 0) return H3GQA_OK;
 
@@ -229,8 +258,13 @@ h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v, void 
         delete prm;
         return H3GQA_ERR_CUDA;
     }
-    prm->o = static_cast<uint16_t *>(o);
+    prm->o = o;
     prm->lse = lse;
+    prm->o_scale = opt.o_scale;
+    prm->causal = opt.causal;
+    prm->out_token_major = opt.out_layout == H3GQA_LAYOUT_TOKEN_MAJOR;
+    prm->out_int8 = opt.out_int8;
+    prm->n_q_heads = n_q_heads;
     prm->total_tokens = T;
     prm->n_units = hp.n_units;
     prm->n_kv_heads = n_kv_heads;
@@ -251,6 +285,14 @@ h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v, void 
                                    reinterpret_cast<cudaStream_t>(stream)>>>(*prm);
     delete prm;
     return cudaGetLastError() == cudaSuccess ? H3GQA_OK : H3GQA_ERR_CUDA;
+}
+
+h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int n_seqs, int n_q_heads,
+                              int n_kv_heads, int head_dim, float scale, h3gqa_stream_t stream)
+{
+    return h3gqa_attention_fwd(q, k, v, o, lse, cu_seqlens, n_seqs, n_q_heads, n_kv_heads,
+                               head_dim, scale, nullptr, stream);
 }
 
 h3gqa_status h3gqa_sync_and_check(h3gqa_stream_t stream)

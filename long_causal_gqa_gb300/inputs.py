@@ -36,6 +36,7 @@ class Workload:
     head_dim: int = 128
     seed: int = 1000
     n_outlier: int = 0          # channels of q and k scaled by 8
+    causal: bool = True         # False: every key of the sequence (bidirectional)
 
     @property
     def total_tokens(self) -> int:
@@ -46,13 +47,16 @@ class Workload:
         return self.head_dim ** -0.5
 
     def metric_flops(self) -> float:
-        """FLOPs as the headline metric counts them: sum_b 2*S_b^2*Hq*D."""
-        return float(sum(2.0 * s * s * self.n_q_heads * self.head_dim
-                         for s in self.seqlens))
+        """FLOPs as the headline metric counts them: sum_b 2*S_b^2*Hq*D
+        (causal), 4*S_b^2*Hq*D without the causal rule."""
+        k = 2.0 if self.causal else 4.0
+        return float(sum(k * s * s * self.n_q_heads * self.head_dim for s in self.seqlens))
 
     def exact_flops(self) -> float:
-        """FLOPs of the causal pairs actually needed: 2*Hq*D*S(S+1) per sequence
-        (one QK^T and one PV multiply-add per visible (query, key) pair)."""
+        """FLOPs of the visible pairs: 4*D per (query, key, head) pair, i.e.
+        2*Hq*D*S(S+1) per sequence when causal."""
+        if not self.causal:
+            return self.metric_flops()
         return float(sum(2.0 * self.n_q_heads * self.head_dim * s * (s + 1)
                          for s in self.seqlens))
 
@@ -68,6 +72,11 @@ WORKLOADS = {
     "s10231": Workload("s10231", (10231,), seed=1003),
     "varlen4": Workload("varlen4", (8184, 8199, 8510, 10231), seed=1004),
     "s32768_outlier": Workload("s32768_outlier", (32768,), seed=1005, n_outlier=4),
+    # Bidirectional attention at the DiT row counts of tgo-app-dev/vpipe
+    # issue #10 (a 19316-row forward and a 34121-row forward), with the
+    # encoder's head shape (a reading: the pages give no DiT head counts).
+    "dit19316": Workload("dit19316", (19316,), seed=1006, causal=False),
+    "dit34121": Workload("dit34121", (34121,), seed=1007, causal=False),
 }
 
 HEADLINE = "s10231"

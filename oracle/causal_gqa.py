@@ -36,6 +36,11 @@ def bind(path):
     lib.oracle_attention_probs.argtypes = common + [
         ctypes.c_int, ctypes.c_int64, f64p]
     lib.oracle_attention_probs.restype = ctypes.c_int64
+    lib.oracle_attention.argtypes = common + [ctypes.c_int, f64p, f64p, ctypes.c_int]
+    lib.oracle_attention.restype = ctypes.c_int
+    lib.oracle_attention_rows.argtypes = common + [
+        ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p, ctypes.c_int]
+    lib.oracle_attention_rows.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -77,15 +82,16 @@ def _ptr(a, ctype):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
-def causal_gqa(q, k, v, cu_seqlens, n_q_heads, n_kv_heads, scale, n_threads=0):
-    """All rows. Returns (o [Hq,T,D] fp64, lse [Hq,T] fp64)."""
+def causal_gqa(q, k, v, cu_seqlens, n_q_heads, n_kv_heads, scale, n_threads=0, causal=True):
+    """All rows. Returns (o [Hq,T,D] fp64, lse [Hq,T] fp64). causal=False gives
+    the bidirectional form (every key of the sequence)."""
     q, k, v, cu, T, D = _prep(q, k, v, cu_seqlens, n_q_heads, n_kv_heads)
     o = np.zeros((n_q_heads, T, D), dtype=np.float64)
     lse = np.zeros((n_q_heads, T), dtype=np.float64)
-    rc = _lib().oracle_causal_gqa(
+    rc = _lib().oracle_attention(
         _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
         _ptr(cu, ctypes.c_int32), len(cu) - 1, n_q_heads, n_kv_heads, D,
-        float(scale), _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+        float(scale), 1 if causal else 0, _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
         int(n_threads))
     if rc != 0:
         raise ValueError("oracle rejected its arguments (code %d)" % rc)
@@ -93,7 +99,7 @@ def causal_gqa(q, k, v, cu_seqlens, n_q_heads, n_kv_heads, scale, n_threads=0):
 
 
 def causal_gqa_rows(q, k, v, cu_seqlens, n_q_heads, n_kv_heads, scale, rows,
-                    n_threads=0):
+                    n_threads=0, causal=True):
     """Selected rows: rows is an int array [n, 2] of (query head, token row).
 
     Returns (o [n,D] fp64, lse [n] fp64)."""
@@ -102,10 +108,10 @@ def causal_gqa_rows(q, k, v, cu_seqlens, n_q_heads, n_kv_heads, scale, rows,
     n = rows.shape[0]
     o = np.zeros((n, D), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
-    rc = _lib().oracle_causal_gqa_rows(
+    rc = _lib().oracle_attention_rows(
         _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
         _ptr(cu, ctypes.c_int32), len(cu) - 1, n_q_heads, n_kv_heads, D,
-        float(scale), _ptr(rows, ctypes.c_int64), n,
+        float(scale), 1 if causal else 0, _ptr(rows, ctypes.c_int64), n,
         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double), int(n_threads))
     if rc != 0:
         raise ValueError("oracle rejected its arguments (code %d)" % rc)

@@ -24,6 +24,11 @@
  *     o[h,i,:] = sum_j exp(z_j - L) * v[g,j,:]
  *     lse[h,i] = L
  *
+ * The bidirectional form (causal = 0) is the same sum over every key of the
+ * sequence, j in [s_b, e_b): the long DiT attention that the h3.c README
+ * ("Metal 4 and TensorOps paths") keeps on MPSGraph and whose 19316- and
+ * 34121-row forwards tgo-app-dev/vpipe issue #10 reports.
+ *
  * Readings where the pages are silent (they give no head mapping, scale,
  * layout or LSE convention):
  *   - contiguous head groups, g = h / (Hq/Hkv) (same as repeating each KV
@@ -84,14 +89,16 @@ static int check_args(const int32_t *cu, int n_seqs, int hq, int hkv, int d)
  * least (i - s_b + 1) doubles; qrow of D doubles. */
 static void one_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                     const int32_t *cu, int n_seqs, int hq, int hkv, int d,
-                    double scale, int64_t T, int h, int64_t i,
+                    double scale, int causal, int64_t T, int h, int64_t i,
                     double *z, double *qrow, double *o_row, double *lse,
                     double *p_row)
 {
     const int b = sequence_of(cu, n_seqs, i);
     const int64_t s_b = cu[b];
+    const int64_t e_b = cu[b + 1];
     const int g = (int)(((int64_t)h * hkv) / hq);
-    const int64_t n = i - s_b + 1;                 /* keys s_b .. i */
+    const int64_t n_causal = i - s_b + 1;          /* keys s_b .. i */
+    const int64_t n = causal ? n_causal : e_b - s_b;
 
     for (int c = 0; c < d; ++c)
         qrow[c] = bf16_bits_to_double(q[((int64_t)h * T + i) * d + c]);
@@ -133,12 +140,13 @@ static int64_t longest_sequence(const int32_t *cu, int n_seqs)
     return best;
 }
 
-/* Every row of every head: o [Hq][T][D], lse [Hq][T], both fp64.
+/* Every row of every head: o [Hq][T][D], lse [Hq][T], both fp64; causal
+ * selects the causal (1) or bidirectional (0) key range.
  * n_threads <= 0 keeps the OpenMP default. Returns 0 on success. */
-int oracle_causal_gqa(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                      const int32_t *cu_seqlens, int n_seqs,
-                      int n_q_heads, int n_kv_heads, int head_dim, double scale,
-                      double *o, double *lse, int n_threads)
+int oracle_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const int32_t *cu_seqlens, int n_seqs,
+                     int n_q_heads, int n_kv_heads, int head_dim, double scale,
+                     int causal, double *o, double *lse, int n_threads)
 {
     int rc = check_args(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim);
     if (rc) return rc;
@@ -165,7 +173,7 @@ int oracle_causal_gqa(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 const int h = (int)(r / T);
                 const int64_t i = r % T;
                 one_row(q, k, v, cu_seqlens, n_seqs, n_q_heads, n_kv_heads,
-                        head_dim, scale, T, h, i, z, qrow,
+                        head_dim, scale, causal, T, h, i, z, qrow,
                         o + r * head_dim, lse + r, NULL);
             }
         }
@@ -177,11 +185,11 @@ int oracle_causal_gqa(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 
 /* A chosen set of rows: rows[2*r] = query head h, rows[2*r+1] = token row t.
  * o_rows [n_rows][D], lse_rows [n_rows], fp64. Returns 0 on success. */
-int oracle_causal_gqa_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                           const int32_t *cu_seqlens, int n_seqs,
-                           int n_q_heads, int n_kv_heads, int head_dim, double scale,
-                           const int64_t *rows, int64_t n_rows,
-                           double *o_rows, double *lse_rows, int n_threads)
+int oracle_attention_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const int32_t *cu_seqlens, int n_seqs,
+                          int n_q_heads, int n_kv_heads, int head_dim, double scale,
+                          int causal, const int64_t *rows, int64_t n_rows,
+                          double *o_rows, double *lse_rows, int n_threads)
 {
     int rc = check_args(cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim);
     if (rc) return rc;
@@ -208,13 +216,33 @@ int oracle_causal_gqa_rows(const uint16_t *q, const uint16_t *k, const uint16_t 
 #pragma omp for schedule(dynamic, 4)
             for (int64_t r = 0; r < n_rows; ++r)
                 one_row(q, k, v, cu_seqlens, n_seqs, n_q_heads, n_kv_heads,
-                        head_dim, scale, T, (int)rows[2 * r], rows[2 * r + 1],
+                        head_dim, scale, causal, T, (int)rows[2 * r], rows[2 * r + 1],
                         z, qrow, o_rows + r * head_dim, lse_rows + r, NULL);
         }
         free(z);
         free(qrow);
     }
     return failed ? 5 : 0;
+}
+
+/* The causal entry points: the definition above with causal = 1. */
+int oracle_causal_gqa(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const int32_t *cu_seqlens, int n_seqs,
+                      int n_q_heads, int n_kv_heads, int head_dim, double scale,
+                      double *o, double *lse, int n_threads)
+{
+    return oracle_attention(q, k, v, cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim,
+                            scale, 1, o, lse, n_threads);
+}
+
+int oracle_causal_gqa_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           const int32_t *cu_seqlens, int n_seqs,
+                           int n_q_heads, int n_kv_heads, int head_dim, double scale,
+                           const int64_t *rows, int64_t n_rows,
+                           double *o_rows, double *lse_rows, int n_threads)
+{
+    return oracle_attention_rows(q, k, v, cu_seqlens, n_seqs, n_q_heads, n_kv_heads,
+                                 head_dim, scale, 1, rows, n_rows, o_rows, lse_rows, n_threads);
 }
 
 /* The probability row of one query (h, t): p_out[j - s_b] = exp(z_j - L) for
@@ -235,7 +263,7 @@ int64_t oracle_attention_probs(const uint16_t *q, const uint16_t *k, const uint1
     double lse;
     if (!z || !qrow || !orow) { free(z); free(qrow); free(orow); return -1; }
     one_row(q, k, v, cu_seqlens, n_seqs, n_q_heads, n_kv_heads, head_dim, scale,
-            T, h, t, z, qrow, orow, &lse, p_out);
+            1, T, h, t, z, qrow, orow, &lse, p_out);
     free(z); free(qrow); free(orow);
     return n;
 }

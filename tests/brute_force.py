@@ -12,8 +12,9 @@ def bf16_bits_to_f64(bits):
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def dense_causal_gqa(q, k, v, cu_seqlens, scale):
-    """q [Hq,T,D], k/v [Hkv,T,D] as float64 arrays. Returns (o, lse, P-list)."""
+def dense_causal_gqa(q, k, v, cu_seqlens, scale, causal=True):
+    """q [Hq,T,D], k/v [Hkv,T,D] as float64 arrays. Returns (o, lse, P-list).
+    causal=False drops the mask (every key of the sequence)."""
     hq, T, D = q.shape
     hkv = k.shape[0]
     rep = hq // hkv
@@ -28,7 +29,7 @@ def dense_causal_gqa(q, k, v, cu_seqlens, scale):
         if n == 0:
             continue
         z = scale * np.einsum("hid,hjd->hij", q[:, s:e], k_full[:, s:e])
-        mask = np.tril(np.ones((n, n), dtype=bool))
+        mask = np.tril(np.ones((n, n), dtype=bool)) if causal else np.ones((n, n), dtype=bool)
         z = np.where(mask[None], z, -np.inf)
         m = z.max(axis=-1, keepdims=True)
         L = m + np.log(np.exp(z - m).sum(axis=-1, keepdims=True))

@@ -143,3 +143,37 @@ def test_library_links_no_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 assert "oracle" not in open(os.path.join(dirpath, f)).read().lower() or \
                     f == "inputs.py", f
+
+
+def test_attention_plan_bidirectional(lib):
+    p = binding.h3gqa_attention_plan([0, 19316], 64, 8, causal=False)
+    tiles = (19316 + 127) // 128
+    assert p.n_units == 8 * ((19316 + 31) // 32)
+    assert p.n_kv_tiles == p.n_units * tiles           # every unit sees every key tile
+    assert p.metric_flops == 4.0 * 64 * 128 * 19316 ** 2
+    assert p.causal_flops == p.metric_flops
+    assert p.exp2_count == 64 * 19316 ** 2
+    c = binding.h3gqa_attention_plan([0, 19316], 64, 8, causal=True)
+    assert c.n_kv_tiles < p.n_kv_tiles and c.n_units == p.n_units
+    assert binding.h3gqa_make_plan([0, 19316], 64, 8).n_kv_tiles == c.n_kv_tiles
+
+
+def test_attention_options_rejected_before_cuda(lib):
+    good = 1 << 20
+    base = dict(q_ptr=good, k_ptr=good, v_ptr=good, o_ptr=good, lse_ptr=good,
+                cu_seqlens=[0, 64], n_q_heads=64, n_kv_heads=8, head_dim=128, scale=0.088)
+    bad_opts = [binding.make_options(out_int8=True),                       # no o_scale
+                binding.make_options(out_int8=True, o_scale_ptr=good + 2),  # misaligned o_scale
+                binding.make_options(out_layout=2),
+                binding.make_options(reserved=1)]
+    o = binding.make_options()
+    o.causal = 2
+    bad_opts.append(o)
+    for opts in bad_opts:
+        assert binding.h3gqa_attention_fwd(options=opts, check=False, **base) == \
+            H3GQA_ERR_INVALID_ARG
+    # valid options with nothing to do return OK without a device
+    ok = binding.make_options(causal=False, out_layout=binding.H3GQA_LAYOUT_TOKEN_MAJOR,
+                              out_int8=True, o_scale_ptr=good)
+    assert binding.h3gqa_attention_fwd(options=ok, check=False,
+                                       **dict(base, cu_seqlens=[0, 0])) == H3GQA_OK

@@ -18,10 +18,12 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 
 # (name, exact text in the oracle, replacement)
 MUTANTS = [
-    ("drops the diagonal key", "const int64_t n = i - s_b + 1;",
-     "const int64_t n = i - s_b + (i > s_b ? 0 : 1);"),
-    ("sees one future key", "const int64_t n = i - s_b + 1;",
-     "const int64_t n = i - s_b + 1 + (i + 1 < cu[b + 1] ? 1 : 0);"),
+    ("drops the diagonal key", "const int64_t n_causal = i - s_b + 1;",
+     "const int64_t n_causal = i - s_b + (i > s_b ? 0 : 1);"),
+    ("sees one future key", "const int64_t n_causal = i - s_b + 1;",
+     "const int64_t n_causal = i - s_b + 1 + (i + 1 < cu[b + 1] ? 1 : 0);"),
+    ("bidirectional rows stop at the query", "const int64_t n = causal ? n_causal : e_b - s_b;",
+     "const int64_t n = causal ? n_causal : n_causal;"),
     ("wrong GQA head (modulo)", "const int g = (int)(((int64_t)h * hkv) / hq);",
      "const int g = h % hkv;"),
     ("scale not applied", "z[jj] = scale * dot;", "z[jj] = dot;"),
@@ -49,6 +51,10 @@ PIN_CALLS = [
     ("gqa-repeat", pins.test_gqa_equals_explicit_kv_repetition),
     ("varlen", pins.test_varlen_equals_separate_calls),
     ("key-shift", pins.test_common_key_shift),
+    ("bidir-brute", lambda: pins.test_bidirectional_matches_dense_bruteforce((17,), 2, 1, 8)),
+    ("bidir-sdpa", pins.test_bidirectional_matches_torch_sdpa_float64),
+    ("bidir-perm", pins.test_bidirectional_is_invariant_to_key_order),
+    ("bidir-zero", pins.test_bidirectional_zero_scale_and_last_row),
 ]
 
 

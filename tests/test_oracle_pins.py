@@ -262,3 +262,70 @@ def test_input_recipe_is_deterministic_and_bf16():
     assert torch.equal(a["outlier_channels"], b["outlier_channels"])
     assert a["cu_seqlens"].tolist() == [0, 5, 8]
     assert cu_seqlens_of([]).tolist() == [0]
+
+
+# ------------------------------------------------------- bidirectional form
+@pytest.mark.parametrize("seqlens,hq,hkv,d", [((17,), 2, 1, 8), ((5, 0, 11, 1, 20), 8, 1, 8),
+                                              ((64,), 8, 2, 128)])
+def test_bidirectional_matches_dense_bruteforce(seqlens, hq, hkv, d):
+    x = make_inputs(seqlens, hq, hkv, d, seed=70 + hq + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv, scale,
+                            causal=False)
+    ob, lb, _ = dense_causal_gqa(_f64(x["q"]), _f64(x["k"]), _f64(x["v"]),
+                                 x["cu_seqlens"].numpy(), scale, causal=False)
+    np.testing.assert_allclose(o, ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lb, rtol=0, atol=1e-12)
+
+
+def test_bidirectional_matches_torch_sdpa_float64():
+    seqlens, hq, hkv, d = (9, 23), 4, 2, 32
+    x = make_inputs(seqlens, hq, hkv, d, seed=71)
+    o, _ = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv, 0.37, causal=False)
+    q, k, v = (torch.from_numpy(_f64(x[n])) for n in ("q", "k", "v"))
+    cu = x["cu_seqlens"].tolist()
+    for b in range(len(cu) - 1):
+        s, e = cu[b], cu[b + 1]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[None, :, s:e], k[None, :, s:e], v[None, :, s:e], is_causal=False, scale=0.37,
+            enable_gqa=True)[0]
+        np.testing.assert_allclose(o[:, s:e], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_bidirectional_is_invariant_to_key_order():
+    """Without the causal rule a row sees a set of keys: permuting the keys
+    and values of a sequence together changes no output (the causal form
+    does change)."""
+    seqlens, hq, hkv, d = (19, 12), 4, 2, 16
+    x = make_inputs(seqlens, hq, hkv, d, seed=72)
+    o, lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv, 0.3, causal=False)
+    perm = np.concatenate([np.random.default_rng(0).permutation(19),
+                           19 + np.random.default_rng(1).permutation(12)])
+    k2, v2 = x["k"][:, perm].contiguous(), x["v"][:, perm].contiguous()
+    o2, lse2 = orc.causal_gqa(x["q"], k2, v2, x["cu_seqlens"], hq, hkv, 0.3, causal=False)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse2, lse, rtol=0, atol=1e-12)
+    oc, _ = orc.causal_gqa(x["q"], k2, v2, x["cu_seqlens"], hq, hkv, 0.3)
+    oc0, _ = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv, 0.3)
+    assert np.abs(oc - oc0).max() > 1e-3
+
+
+def test_bidirectional_zero_scale_and_last_row():
+    """scale = 0: every row of a sequence is the mean of all its values and
+    lse = ln(S_b); and in general the last row of a sequence is the same in
+    both forms (it sees every key either way)."""
+    seqlens, hq, hkv, d = (10, 25), 4, 1, 8
+    x = make_inputs(seqlens, hq, hkv, d, seed=73)
+    o, lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv, 0.0, causal=False)
+    v = _f64(x["v"])
+    cu = x["cu_seqlens"].tolist()
+    for b in range(len(seqlens)):
+        s, e = cu[b], cu[b + 1]
+        np.testing.assert_allclose(o[:, s:e], np.broadcast_to(v[0, s:e].mean(0), o[:, s:e].shape),
+                                   rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, s:e], math.log(e - s), rtol=0, atol=1e-13)
+    ob, lb = orc.causal_gqa(x["q"], x["k"], x["v"], cu, hq, hkv, 0.4, causal=False)
+    oc, lc = orc.causal_gqa(x["q"], x["k"], x["v"], cu, hq, hkv, 0.4)
+    for e in cu[1:]:
+        np.testing.assert_array_equal(ob[:, e - 1], oc[:, e - 1])
+        np.testing.assert_array_equal(lb[:, e - 1], lc[:, e - 1])
