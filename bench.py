@@ -28,19 +28,21 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from long_causal_gqa_gb300 import binding  # noqa: E402
-from long_causal_gqa_gb300.inputs import HEADLINE, WORKLOADS, make_workload_inputs  # noqa: E402
+from long_causal_gqa_gb300.inputs import (HEADLINE, WORKLOADS, make_workload_inputs,  # noqa: E402
+                                         norm_weights, rope_tables)
 
 METRIC = "causal GQA prefill TFLOP/s at S=10231 (Hq64/Hkv8/D128), % of BF16 peak"
 EPILOGUES = {"bf16_head": (False, False), "bf16_token": (True, False), "int8_token": (True, True),
              "int8_head": (False, True)}
 
 
-def metric_name(w, epilogue):
-    if w.name == HEADLINE and epilogue == "bf16_head":
+def metric_name(w, epilogue, prologue=False):
+    if w.name == HEADLINE and epilogue == "bf16_head" and not prologue:
         return METRIC
     kind = "causal GQA prefill" if w.causal else "bidirectional GQA attention"
-    return "%s TFLOP/s, workload %s (Hq%d/Hkv%d/D%d), output %s" % (
-        kind, w.name, w.n_q_heads, w.n_kv_heads, w.head_dim, epilogue)
+    return "%s TFLOP/s, workload %s (Hq%d/Hkv%d/D%d), output %s%s" % (
+        kind, w.name, w.n_q_heads, w.n_kv_heads, w.head_dim, epilogue,
+        ", with Q/K RMS-norm + RoPE prologue" if prologue else "")
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -232,10 +234,19 @@ def run_ours(args, world, rank, local):
     lse = torch.empty((w.n_q_heads, w.total_tokens), dtype=torch.float32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     sh = stream.cuda_stream
-    default_call = w.causal and args.epilogue == "bf16_head"
-    opts = binding.make_options(w.causal, binding.H3GQA_LAYOUT_TOKEN_MAJOR if token_major
-                                else binding.H3GQA_LAYOUT_HEAD_MAJOR, out_int8,
-                                o_scale.data_ptr() if o_scale is not None else None)
+    default_call = w.causal and args.epilogue == "bf16_head" and not args.prologue
+    pro = {}
+    if args.prologue:
+        wq, wk = norm_weights(w.head_dim, w.seed)
+        cos, sin = rope_tables(w.seqlens, w.head_dim)
+        pro = dict(wq=wq.to(device), wk=wk.to(device), cos=cos.to(device), sin=sin.to(device),
+                   k_out=torch.empty_like(k))
+    opts = binding.make_options(
+        w.causal, binding.H3GQA_LAYOUT_TOKEN_MAJOR if token_major
+        else binding.H3GQA_LAYOUT_HEAD_MAJOR, out_int8,
+        o_scale.data_ptr() if o_scale is not None else None, 0,
+        *([pro["wq"].data_ptr(), pro["wk"].data_ptr(), pro["cos"].data_ptr(),
+           pro["sin"].data_ptr(), pro["k_out"].data_ptr()] if pro else []))
 
     def launch():
         if default_call:
@@ -311,28 +322,30 @@ def run_ours(args, world, rank, local):
     value = whole_job_value(w.metric_flops(), world, ms_max)
     achieved = plan.causal_flops / (ms * 1e-3) / 1e12
     line = {
-        "metric": metric_name(w, args.epilogue), "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": metric_name(w, args.epilogue, args.prologue), "value": value, "unit": UNIT,
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q/k/v; no dataset)",
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "config": {"workload": w.name, "seqlens": list(w.seqlens), "n_q_heads": w.n_q_heads,
                    "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "causal": w.causal,
-                   "output": args.epilogue,
+                   "output": args.epilogue, "qk_prologue": bool(args.prologue),
                    "scale": w.scale, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed before every step (256 MB write, outside the kernel events)",
                    "flops_per_step_metric": w.metric_flops(),
                    "flops_per_step_causal_exact": plan.causal_flops},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak,
-                     "traffic": kernel_traffic(w.name) if args.epilogue == "bf16_head" else None,
+                     "traffic": kernel_traffic(w.name)
+                     if args.epilogue == "bf16_head" and not args.prologue else None,
                      "traffic_unit": "bytes per launch (ncu dram read+write)",
                      "peak_source": "%s bf16_tflops (burst)" % peak_src,
                      "kernel": "h3gqa::causal_gqa_fwd_kernel",
                      "work": "4*D FLOPs per visible (query, key, head) pair per launch"},
         "e2e": {"value": whole_job_value(w.metric_flops(), world, e2e_ms), "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if args.prologue else 1),
         "clocks": sampler.summary(t0, t1),
         "kernel_ms": {"mean": ms, "min": float(np.min(times)), "max": float(np.max(times))},
     }
@@ -352,6 +365,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--epilogue", choices=sorted(EPILOGUES), default="bf16_head",
                     help="output form: bf16 or int8 codes (+ per-row scales), head- or token-major")
+    ap.add_argument("--prologue", action="store_true",
+                    help="add the Q/K RMS-norm + rotary prologue (K pass + Q in-kernel)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -117,14 +117,39 @@ typedef struct {
     int32_t out_int8;      /* 0: o is bf16; 1: o is int8 codes plus o_scale */
     int32_t reserved;      /* must be 0 */
     float *o_scale;        /* device fp32 [Hq][T] or [T][Hq], 4-byte aligned; required iff out_int8 */
+    /* Q/K prologue (see below); all null = inputs are used as given. */
+    const void *q_norm_weight;   /* device bf16 [head_dim], 16-byte aligned, or null */
+    const void *k_norm_weight;   /* device bf16 [head_dim], 16-byte aligned, or null */
+    const float *rope_cos;       /* device fp32 [T][head_dim/2], 16-byte aligned, or null */
+    const float *rope_sin;       /* same shape; given together with rope_cos */
+    void *k_out;                 /* device bf16 [Hkv][T][head_dim], 16-byte aligned: receives the
+                                    prepared keys; required iff k is prepared; may equal k */
+    float norm_eps;              /* added to the mean square; finite and >= 0 */
+    int32_t reserved2;           /* must be 0 */
 } h3gqa_options;
+
+/*
+ * Q/K prologue (h3.c README, "Profiling and diagnostic paths" and
+ * "Checkpoint layout and media pipeline": the fused Q/K normalisation and
+ * rotary embedding that precedes attention). With a norm weight w, every
+ * (head, token) row x of q (k) becomes x * rsqrt(mean(x^2) + norm_eps) * w;
+ * with rope tables, then, for i < head_dim/2 and token t,
+ *   (y_i, y_{i+D/2}) <- (y_i cos[t][i] - y_{i+D/2} sin[t][i],
+ *                        y_{i+D/2} cos[t][i] + y_i sin[t][i])
+ * (the rotate-half pairing; the tables carry any position scheme). The result
+ * is rounded to bf16 once. The rotation applies to q and k; the norms to
+ * whichever has a weight. q is transformed on the fly in the attention
+ * kernel (q itself is not modified); k is transformed once into k_out, which
+ * the attention then reads.
+ */
 
 /*
  * h3gqa_causal_fwd with options (NULL options = causal, head-major bf16 o,
  * i.e. exactly h3gqa_causal_fwd). Arguments and errors as for
  * h3gqa_causal_fwd; in addition an options value outside the ranges above,
- * or out_int8 without a valid o_scale, returns H3GQA_ERR_INVALID_ARG. lse is
- * always [Hq][T].
+ * out_int8 without a valid o_scale, a misaligned prologue pointer, rope_cos
+ * without rope_sin (or the reverse) or a prepared k without k_out returns
+ * H3GQA_ERR_INVALID_ARG. lse is always [Hq][T].
  */
 h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v,
                                  void *o, float *lse,

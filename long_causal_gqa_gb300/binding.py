@@ -55,6 +55,13 @@ class h3gqa_options(ctypes.Structure):
         ("out_int8", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
         ("o_scale", ctypes.c_void_p),
+        ("q_norm_weight", ctypes.c_void_p),
+        ("k_norm_weight", ctypes.c_void_p),
+        ("rope_cos", ctypes.c_void_p),
+        ("rope_sin", ctypes.c_void_p),
+        ("k_out", ctypes.c_void_p),
+        ("norm_eps", ctypes.c_float),
+        ("reserved2", ctypes.c_int32),
     ]
 
 
@@ -132,9 +139,12 @@ def h3gqa_attention_plan(cu_seqlens, n_q_heads, n_kv_heads, head_dim=128, causal
 
 
 def make_options(causal=True, out_layout=H3GQA_LAYOUT_HEAD_MAJOR, out_int8=False,
-                 o_scale_ptr=None, reserved=0):
+                 o_scale_ptr=None, reserved=0, q_norm_ptr=None, k_norm_ptr=None, cos_ptr=None,
+                 sin_ptr=None, k_out_ptr=None, norm_eps=1e-6, reserved2=0):
     return h3gqa_options(1 if causal else 0, int(out_layout), 1 if out_int8 else 0,
-                         int(reserved), o_scale_ptr or None)
+                         int(reserved), o_scale_ptr or None, q_norm_ptr or None,
+                         k_norm_ptr or None, cos_ptr or None, sin_ptr or None,
+                         k_out_ptr or None, float(norm_eps), int(reserved2))
 
 
 def h3gqa_attention_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, cu_seqlens, n_q_heads, n_kv_heads,
@@ -171,10 +181,14 @@ def h3gqa_sync_and_check(stream=0, check=True):
 
 
 def attention_fwd(q, k, v, cu_seqlens, scale=None, causal=True, token_major=False,
-                  out_int8=False, stream=None):
+                  out_int8=False, stream=None, q_norm_weight=None, k_norm_weight=None,
+                  rope_cos=None, rope_sin=None, norm_eps=1e-6, k_out=None):
     """Torch front end of h3gqa_attention_fwd. Returns (o, lse, o_scale):
     o bf16 (or int8 codes) in [Hq,T,D] or [T,Hq,D] order, lse fp32 [Hq,T],
-    o_scale fp32 [Hq,T] / [T,Hq] for int8 output (else None)."""
+    o_scale fp32 [Hq,T] / [T,Hq] for int8 output (else None). With the Q/K
+    prologue (norm weights: bf16 [D] CUDA; rope tables: fp32 [T, D/2] CUDA)
+    the prepared keys go to k_out (allocated if not given; read it back as
+    the post-prologue key cache)."""
     import torch
     if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
         raise ValueError("q, k, v must be [heads, T, head_dim]")
@@ -191,9 +205,18 @@ def attention_fwd(q, k, v, cu_seqlens, scale=None, causal=True, token_major=Fals
     o_scale = None
     if out_int8:
         o_scale = torch.empty(shape[:2], dtype=torch.float32, device=q.device)
+    prep_k = k_norm_weight is not None or rope_cos is not None
+    if prep_k and k_out is None:
+        k_out = torch.empty_like(k)
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    for name, t in (("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight),
+                    ("rope_cos", rope_cos), ("rope_sin", rope_sin)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
     opts = make_options(causal, H3GQA_LAYOUT_TOKEN_MAJOR if token_major else
-                        H3GQA_LAYOUT_HEAD_MAJOR, out_int8,
-                        o_scale.data_ptr() if o_scale is not None else None)
+                        H3GQA_LAYOUT_HEAD_MAJOR, out_int8, ptr(o_scale), 0, ptr(q_norm_weight),
+                        ptr(k_norm_weight), ptr(rope_cos), ptr(rope_sin),
+                        ptr(k_out) if prep_k else None, norm_eps)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     h3gqa_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),

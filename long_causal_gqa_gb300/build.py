@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = [os.path.join(CSRC, "h3gqa_api.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fwd_kernel.cuh", "ptx_sm103a.cuh")] + [
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fwd_kernel.cuh", "ptx_sm103a.cuh", "prep_kernel.cuh")] + [
     os.path.join(INCLUDE, "h3gqa.h")]
 LIB = os.path.join(HERE, "libh3gqa.so")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -43,11 +43,15 @@ constexpr uint32_t kSubTileBytes = 128 * 128;          // 128 rows x 64 bf16 (on
 constexpr uint32_t kTileBytes = 2 * kSubTileBytes;     // 128 rows x 128 bf16
 constexpr uint32_t kQOff = 0;                          // two query tiles
 constexpr uint32_t kKvOff = kQOff + 2 * kTileBytes;
-constexpr uint32_t kBarOff = kKvOff + kStages * kTileBytes;
+constexpr uint32_t kRopeOff = kKvOff + kStages * kTileBytes;   // cos rows, then sin rows, of one unit
+constexpr uint32_t kRopeRowBytes = kHeadDim / 2 * 4;           // 64 fp32 per token
+constexpr int kRopeMaxTokens = 32;                             // staged when a unit has <= 32 tokens (G >= 8)
+constexpr uint32_t kRopeBytes = 2 * kRopeMaxTokens * kRopeRowBytes;
+constexpr uint32_t kBarOff = kRopeOff + kRopeBytes;
 // barrier slots
 constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + kStages,
               kBarSFull = 2 + 2 * kStages, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2,
-              kBarDrain = kBarOFull + 2, kNumBars = kBarDrain + 2;
+              kBarDrain = kBarOFull + 2, kBarQReady = kBarDrain + 2, kNumBars = kBarQReady + 2;
 constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag, [2..3] MMA turn counters
 constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 512;
@@ -73,6 +77,14 @@ struct FwdParams {
     int out_token_major;    // 0: o is [Hq][T][128]; 1: o is [T][Hq][128] (o_scale likewise)
     int out_int8;           // 0: bf16 o; 1: int8 codes, o ~= code * o_scale
     int n_q_heads;
+    // Q prologue (RMS-norm and/or rotary embedding applied to each Q tile in
+    // shared memory right after it lands): prep_q != 0 enables it.
+    int prep_q;
+    int stage_rope;             // rotary rows of each unit copied into shared memory with its Q
+    const uint16_t *q_norm_w;   // bf16 [128] or null
+    const float *rope_cos;      // fp32 [T][64] or null
+    const float *rope_sin;
+    float norm_eps;
     long long total_tokens;
     long long n_units;
     int n_kv_heads;
@@ -252,6 +264,8 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             mbar_init(bar(kBarPFull + t), kRows);
             mbar_init(bar(kBarOFull + t), 1);
         }
+        mbar_init(bar(kBarQReady), kRows);
+        mbar_init(bar(kBarQReady + 1), kRows);
         mbar_init(bar(kBarDrain), 1);
         mbar_init(bar(kBarDrain + 1), 1);
         *abort_flag = 0;
@@ -288,8 +302,19 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 const int tb = un.block * p.unit_tokens;
                 const int n_kv = unit_kv_tiles(p, un);
                 if (!wait_poll(bar(kBarQEmpty), (unit_it & 1) ^ 1, abort_flag, 1u)) { ok = false; break; }
-                mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+                uint32_t rope_bytes = 0;
+                const long long tok0 = (long long)un.seq_start + tb;
+                if (p.stage_rope) {
+                    const long long rows = min((long long)p.unit_tokens, p.total_tokens - tok0);
+                    rope_bytes = (uint32_t)rows * kRopeRowBytes;
+                }
+                mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes + 2 * rope_bytes);
                 last_q_parity = unit_it & 1;
+                if (rope_bytes != 0) {
+                    bulk_load(sbase + kRopeOff, p.rope_cos + tok0 * (kHeadDim / 2), rope_bytes, bar(kBarQFull));
+                    bulk_load(sbase + kRopeOff + kRopeBytes / 2, p.rope_sin + tok0 * (kHeadDim / 2), rope_bytes,
+                              bar(kBarQFull));
+                }
                 for (int t = 0; t < 2; ++t)
                     for (int h = 0; h < 2; ++h)
                         tma_load_3d(sQ + (uint32_t)(t * 2 + h) * kSubTileBytes, &p.map_q,
@@ -404,7 +429,10 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 if (u >= p.n_units) break;
                 const Unit un = w.seek(p, u);
                 const int n_kv = unit_kv_tiles(p, un);
-                if (!wait_poll(bar(kBarQFull), unit_it & 1, abort_flag, who)) { ok = false; break; }
+                if (!wait_poll(bar(p.prep_q ? kBarQReady + t : kBarQFull), unit_it & 1, abort_flag, who)) {
+                    ok = false;
+                    break;
+                }
                 {
                     const uint32_t s = kv_it % kStages;
                     if (!wait_poll(bar(kBarKvFull + s), (kv_it / kStages) & 1, abort_flag, who)) { ok = false; break; }
@@ -454,10 +482,100 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
         const int head_in_group = row >> p.tile_tokens_log2;
         const int tok_in_tile = row & (p.tile_tokens - 1);
         const float c = p.scale_log2;
+        // Q prologue for this thread's row of query tile t of unit `uq`: wait
+        // for the tile, RMS-normalise the row and/or rotate it in place in
+        // shared memory, then hand the tile to the MMA issuer (the writes go
+        // through the generic proxy, the MMA reads through the async proxy).
+        auto prep_q = [&](const Unit &uq, uint32_t q_it) -> bool {
+            if (!wait_warp(bar(kBarQFull), q_it & 1, abort_flag, 4u)) return false;
+            const long long tokg = (long long)uq.seq_start + uq.block * p.unit_tokens +
+                                   t * p.tile_tokens + tok_in_tile;
+            if (tokg < p.total_tokens) {
+                uint8_t *rowp = smem + kQOff + (uint32_t)t * kTileBytes + (uint32_t)row * 128u;
+                // 16-byte chunk cc (8 values) of half h of this row, in the
+                // 128-byte swizzled layout TMA wrote
+                auto chunk = [&](int h, int cc) -> uint4 * {
+                    return reinterpret_cast<uint4 *>(rowp + (uint32_t)h * kSubTileBytes +
+                                                     (uint32_t)((cc ^ (row & 7)) << 4));
+                };
+                auto unpack = [](const uint4 v, float (&f)[8]) {
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        f[2 * e] = __uint_as_float(wv[e] << 16);
+                        f[2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
+                    }
+                };
+                float rs = 1.0f;
+                if (p.q_norm_w != nullptr) {
+                    float ss = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int cc = 0; cc < 8; ++cc) {
+                            float f[8];
+                            unpack(*chunk(h, cc), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                        }
+                    rs = rsqrtf(ss * (1.0f / kHeadDim) + p.norm_eps);
+                }
+                // element i of the first half pairs with element i + 64 for the
+                // rotation, so chunk cc of both halves is processed together
+#pragma unroll 2
+                for (int cc = 0; cc < 8; ++cc) {
+                    float a[8], b[8];
+                    unpack(*chunk(0, cc), a);
+                    unpack(*chunk(1, cc), b);
+                    if (p.q_norm_w != nullptr) {
+                        const uint4 wa = __ldg(reinterpret_cast<const uint4 *>(p.q_norm_w) + cc);
+                        const uint4 wb = __ldg(reinterpret_cast<const uint4 *>(p.q_norm_w) + 8 + cc);
+                        float fa[8], fb[8];
+                        unpack(wa, fa);
+                        unpack(wb, fb);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            a[e] = a[e] * rs * fa[e];
+                            b[e] = b[e] * rs * fb[e];
+                        }
+                    }
+                    if (p.rope_cos != nullptr) {
+                        float4 c0, c1, s0, s1;
+                        if (p.stage_rope) {
+                            const float4 *cs4 = reinterpret_cast<const float4 *>(
+                                smem + kRopeOff + (uint32_t)(t * p.tile_tokens + tok_in_tile) * kRopeRowBytes) + 2 * cc;
+                            const float4 *sn4 = cs4 + kRopeBytes / 2 / 16;
+                            c0 = cs4[0]; c1 = cs4[1]; s0 = sn4[0]; s1 = sn4[1];
+                        } else {
+                            const float4 *cs4 = reinterpret_cast<const float4 *>(p.rope_cos + tokg * (kHeadDim / 2) + 8 * cc);
+                            const float4 *sn4 = reinterpret_cast<const float4 *>(p.rope_sin + tokg * (kHeadDim / 2) + 8 * cc);
+                            c0 = __ldg(cs4); c1 = __ldg(cs4 + 1); s0 = __ldg(sn4); s1 = __ldg(sn4 + 1);
+                        }
+                        const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                        const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float x0 = a[e], x1 = b[e];
+                            a[e] = x0 * cs[e] - x1 * sn[e];
+                            b[e] = x1 * cs[e] + x0 * sn[e];
+                        }
+                    }
+                    *chunk(0, cc) = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                               pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+                    *chunk(1, cc) = make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]),
+                                               pack_bf16x2(b[4], b[5]), pack_bf16x2(b[6], b[7]));
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarQReady + t));
+            return true;
+        };
+
         UnitWalker w;
         w.init(p);
-        uint32_t s_phase = 0, o_phase = 0;
+        uint32_t s_phase = 0, o_phase = 0, q_it = 0;
         bool ok = true;
+        if (p.prep_q && unit_of_round(0) < p.n_units) ok = prep_q(w.seek(p, unit_of_round(0)), 0);
         for (long long r = 0; ok; ++r) {
             const long long u = unit_of_round(r);
             if (u >= p.n_units) break;
@@ -540,6 +658,25 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 mbar_arrive(bar(kBarPFull + t));
             }
             if (!ok) break;
+            // The next unit's Q tile lands while this unit's last P.V and the
+            // epilogue run; its rotary table rows are pulled into L1 now.
+            ++q_it;
+            const bool prep_next = p.prep_q && unit_of_round(r + 1) < p.n_units;
+            Unit next_un;
+            if (prep_next) {
+                next_un = w.seek(p, unit_of_round(r + 1));
+                if (p.rope_cos != nullptr && !p.stage_rope) {
+                    const long long tn = (long long)next_un.seq_start + next_un.block * p.unit_tokens +
+                                         t * p.tile_tokens + tok_in_tile;
+                    if (tn < p.total_tokens) {
+#pragma unroll
+                        for (int li = 0; li < 2; ++li) {
+                            prefetch_l1(p.rope_cos + tn * (kHeadDim / 2) + li * 32);
+                            prefetch_l1(p.rope_sin + tn * (kHeadDim / 2) + li * 32);
+                        }
+                    }
+                }
+            }
             // ------------------------------------------------------ epilogue
             if (!wait_warp(bar(kBarOFull + t), o_phase & 1, abort_flag, 4u)) { ok = false; break; }
             ++o_phase;
@@ -605,6 +742,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             }
             if (valid) p.lse[grow] = (m + __log2f(l)) * 0.69314718055994531f;
             tc_fence_before_sync();
+            if (prep_next && !prep_q(next_un, q_it)) { ok = false; break; }
         }
     }
 

@@ -12,6 +12,7 @@
 
 #include "../../include/h3gqa.h"
 #include "fwd_kernel.cuh"
+#include "prep_kernel.cuh"
 
 namespace {
 
@@ -223,8 +224,19 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
                                  int n_kv_heads, int head_dim, float scale,
                                  const h3gqa_options *options, h3gqa_stream_t stream)
 {
-    h3gqa_options opt = {1, H3GQA_LAYOUT_HEAD_MAJOR, 0, 0, nullptr};
+    h3gqa_options opt;
+    std::memset(&opt, 0, sizeof(opt));
+    opt.causal = 1;
+    opt.out_layout = H3GQA_LAYOUT_HEAD_MAJOR;
     if (options != nullptr) opt = *options;
+    const bool prep_k = opt.k_norm_weight != nullptr || opt.rope_cos != nullptr;
+    const bool prep_q = opt.q_norm_weight != nullptr || opt.rope_cos != nullptr;
+    if ((opt.rope_cos == nullptr) != (opt.rope_sin == nullptr) || opt.reserved2 != 0 ||
+        !aligned(opt.q_norm_weight, 16) || !aligned(opt.k_norm_weight, 16) ||
+        !aligned(opt.rope_cos, 16) || !aligned(opt.rope_sin, 16) ||
+        (prep_k && (opt.k_out == nullptr || !aligned(opt.k_out, 16))) ||
+        !(opt.norm_eps >= 0.0f) || !std::isfinite(opt.norm_eps))
+        return H3GQA_ERR_INVALID_ARG;
     if ((opt.causal != 0 && opt.causal != 1) || opt.reserved != 0 ||
         (opt.out_layout != H3GQA_LAYOUT_HEAD_MAJOR && opt.out_layout != H3GQA_LAYOUT_TOKEN_MAJOR) ||
         (opt.out_int8 != 0 && opt.out_int8 != 1))
@@ -248,12 +260,26 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
     st = device_setup(dev, &ds);
     if (st != H3GQA_OK) return st;
 
+    const long long T = hp.total_tokens;
+    const void *k_used = k;
+    if (prep_k) {
+        // keys once, into k_out, before the attention reads them
+        const long long rows = (long long)n_kv_heads * T;
+        // one row per warp: every row's loads are in flight at once
+        const long long blocks = std::min<long long>((rows + 7) / 8, 1LL << 30);
+        h3gqa::qk_prep_kernel<<<(unsigned)blocks, h3gqa::kPrepThreads, 0,
+                                reinterpret_cast<cudaStream_t>(stream)>>>(
+            static_cast<const uint16_t *>(k), static_cast<uint16_t *>(opt.k_out), rows, T,
+            static_cast<const uint16_t *>(opt.k_norm_weight), opt.norm_eps, opt.rope_cos,
+            opt.rope_sin);
+        if (cudaGetLastError() != cudaSuccess) return H3GQA_ERR_CUDA;
+        k_used = opt.k_out;
+    }
     FwdParams *prm = new (std::nothrow) FwdParams;
     if (prm == nullptr) return H3GQA_ERR_CUDA;
     std::memset(prm, 0, sizeof(*prm));
-    const long long T = hp.total_tokens;
     if (!encode_map(&prm->map_q, q, n_q_heads, T, hp.tile_tokens, hp.group) ||
-        !encode_map(&prm->map_k, k, n_kv_heads, T, h3gqa::kKeys, 1) ||
+        !encode_map(&prm->map_k, k_used, n_kv_heads, T, h3gqa::kKeys, 1) ||
         !encode_map(&prm->map_v, v, n_kv_heads, T, h3gqa::kKeys, 1)) {
         delete prm;
         return H3GQA_ERR_CUDA;
@@ -265,6 +291,12 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
     prm->out_token_major = opt.out_layout == H3GQA_LAYOUT_TOKEN_MAJOR;
     prm->out_int8 = opt.out_int8;
     prm->n_q_heads = n_q_heads;
+    prm->prep_q = prep_q ? 1 : 0;
+    prm->stage_rope = (opt.rope_cos != nullptr && hp.unit_tokens <= h3gqa::kRopeMaxTokens) ? 1 : 0;
+    prm->q_norm_w = static_cast<const uint16_t *>(opt.q_norm_weight);
+    prm->rope_cos = opt.rope_cos;
+    prm->rope_sin = opt.rope_sin;
+    prm->norm_eps = opt.norm_eps;
     prm->total_tokens = T;
     prm->n_units = hp.n_units;
     prm->n_kv_heads = n_kv_heads;

@@ -127,6 +127,29 @@ def make_inputs(seqlens, n_q_heads: int, n_kv_heads: int, head_dim: int,
     }
 
 
+def rope_tables(seqlens, head_dim: int, theta: float = 1.0e6):
+    """Rotary tables [T, D/2] fp32 for positions counted from each sequence
+    start: angle = pos * theta^(-2i/D), i < D/2 (the standard rotate-half
+    frequencies; theta = 1e6 as in Qwen3 text models)."""
+    half = head_dim // 2
+    inv = theta ** (-np.arange(half, dtype=np.float64) * 2.0 / head_dim)
+    pos = np.concatenate([np.arange(int(s), dtype=np.float64) for s in seqlens]) \
+        if len(seqlens) else np.zeros(0)
+    ang = pos[:, None] * inv[None, :]
+    return (torch.from_numpy(np.cos(ang).astype(np.float32)),
+            torch.from_numpy(np.sin(ang).astype(np.float32)))
+
+
+def norm_weights(head_dim: int, seed: int):
+    """Synthetic RMS-norm weights for q and k: 1 + 0.1 N(0,1), bf16 (there is no
+    checkpoint); drawn from their own generator so the q/k/v draws are
+    unchanged."""
+    rng = np.random.default_rng(int(seed) + 7919)
+    w = 1.0 + 0.1 * rng.standard_normal((2, head_dim))
+    t = torch.from_numpy(w.astype(np.float32)).to(torch.bfloat16)
+    return t[0].contiguous(), t[1].contiguous()
+
+
 def make_workload_inputs(w: Workload):
     return make_inputs(w.seqlens, w.n_q_heads, w.n_kv_heads, w.head_dim,
                        w.seed, w.n_outlier)

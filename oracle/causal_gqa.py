@@ -41,6 +41,10 @@ def bind(path):
     lib.oracle_attention_rows.argtypes = common + [
         ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p, ctypes.c_int]
     lib.oracle_attention_rows.restype = ctypes.c_int
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_qk_prep.argtypes = [u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, u16p,
+                                   ctypes.c_double, f32p, f32p, f64p]
+    lib.oracle_qk_prep.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -129,6 +133,36 @@ def attention_probs(q, k, v, cu_seqlens, n_q_heads, n_kv_heads, scale, h, t):
     if n < 0:
         raise ValueError("oracle rejected its arguments")
     return p[:n].copy()
+
+
+def qk_prep(x, w=None, eps=1e-6, rope_cos=None, rope_sin=None):
+    """Q/K prologue of every row of x [heads, T, D] (bf16): RMS norm with
+    weight w (bf16 [D], optional) and rotate-half rotary embedding with fp32
+    tables [T, D/2] (optional). Returns fp64 [heads, T, D] (unrounded)."""
+    xb = as_bf16_bits(x)
+    heads, T, D = xb.shape
+    out = np.zeros((heads, T, D), dtype=np.float64)
+    wb = as_bf16_bits(w) if w is not None else None
+    cs = sn = None
+    if rope_cos is not None:
+        cs = np.ascontiguousarray(np.asarray(rope_cos, dtype=np.float32))
+        sn = np.ascontiguousarray(np.asarray(rope_sin, dtype=np.float32))
+        if cs.shape != (T, D // 2) or sn.shape != (T, D // 2):
+            raise ValueError("rope tables must be [T, D/2]")
+    rc = _lib().oracle_qk_prep(
+        _ptr(xb, ctypes.c_uint16), heads * T, T, D,
+        _ptr(wb, ctypes.c_uint16) if wb is not None else None, float(eps),
+        _ptr(cs, ctypes.c_float) if cs is not None else None,
+        _ptr(sn, ctypes.c_float) if sn is not None else None, _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (code %d)" % rc)
+    return out
+
+
+def to_bf16(a):
+    """fp64 array -> bf16 torch tensor: rounded to fp32, then to bf16 (nearest even)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.float32))).to(torch.bfloat16)
 
 
 def max_threads():

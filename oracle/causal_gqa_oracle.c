@@ -268,6 +268,48 @@ int64_t oracle_attention_probs(const uint16_t *q, const uint16_t *k, const uint1
     return n;
 }
 
+/*
+ * Q/K prologue, the step before attention that the h3.c README names
+ * ("Profiling and diagnostic paths", "Checkpoint layout and media
+ * pipeline": fused QK normalisation and rotary embedding). For every row x
+ * (rows = heads * T, token t = row mod T) of a [heads][T][D] bf16 tensor:
+ *   RMS norm (if w): y = x / sqrt(mean_c x_c^2 + eps) * w
+ *   rotation (if tables): for i < D/2, with c = cos[t][i], s = sin[t][i],
+ *     out_i       = y_i c - y_{i+D/2} s
+ *     out_{i+D/2} = y_{i+D/2} c + y_i s
+ * in fp64 (the caller rounds to bf16). Returns 0 on success.
+ */
+int oracle_qk_prep(const uint16_t *x, int64_t rows, int64_t T, int d,
+                   const uint16_t *w, double eps, const float *cosv, const float *sinv,
+                   double *out)
+{
+    if (!x || !out || rows < 0 || T <= 0 || d < 2 || (d % 2) != 0) return 1;
+    if ((cosv == NULL) != (sinv == NULL)) return 2;
+    const int half = d / 2;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t t = r % T;
+        double *y = out + r * d;
+        for (int c = 0; c < d; ++c) y[c] = bf16_bits_to_double(x[r * d + c]);
+        if (w) {
+            double ms = 0.0;
+            for (int c = 0; c < d; ++c) ms += y[c] * y[c];
+            ms /= d;
+            const double inv = 1.0 / sqrt(ms + eps);
+            for (int c = 0; c < d; ++c) y[c] = y[c] * inv * bf16_bits_to_double(w[c]);
+        }
+        if (cosv) {
+            for (int i = 0; i < half; ++i) {
+                const double cs = cosv[t * half + i], sn = sinv[t * half + i];
+                const double a = y[i], b = y[i + half];
+                y[i] = a * cs - b * sn;
+                y[i + half] = b * cs + a * sn;
+            }
+        }
+    }
+    return 0;
+}
+
 /* Threads the OpenMP runtime would use (for reporting the baseline's cores). */
 int oracle_max_threads(void)
 {

@@ -177,3 +177,26 @@ def test_attention_options_rejected_before_cuda(lib):
                               out_int8=True, o_scale_ptr=good)
     assert binding.h3gqa_attention_fwd(options=ok, check=False,
                                        **dict(base, cu_seqlens=[0, 0])) == H3GQA_OK
+
+
+def test_prologue_options_rejected_before_cuda(lib):
+    good = 1 << 20
+    base = dict(q_ptr=good, k_ptr=good, v_ptr=good, o_ptr=good, lse_ptr=good,
+                cu_seqlens=[0, 64], n_q_heads=64, n_kv_heads=8, head_dim=128, scale=0.088)
+    bad = [binding.make_options(cos_ptr=good, sin_ptr=None, k_out_ptr=good),   # cos without sin
+           binding.make_options(cos_ptr=None, sin_ptr=good),                   # sin without cos
+           binding.make_options(cos_ptr=good, sin_ptr=good),                   # k prepared, no k_out
+           binding.make_options(k_norm_ptr=good),                              # likewise
+           binding.make_options(k_norm_ptr=good, k_out_ptr=good + 8),          # misaligned k_out
+           binding.make_options(q_norm_ptr=good + 2),                          # misaligned weight
+           binding.make_options(cos_ptr=good + 4, sin_ptr=good, k_out_ptr=good),
+           binding.make_options(q_norm_ptr=good, norm_eps=-1.0),
+           binding.make_options(q_norm_ptr=good, norm_eps=float("nan")),
+           binding.make_options(reserved2=3)]
+    for opts in bad:
+        assert binding.h3gqa_attention_fwd(options=opts, check=False, **base) == \
+            H3GQA_ERR_INVALID_ARG
+    ok = binding.make_options(q_norm_ptr=good, k_norm_ptr=good, cos_ptr=good, sin_ptr=good,
+                              k_out_ptr=good)
+    assert binding.h3gqa_attention_fwd(options=ok, check=False,
+                                       **dict(base, cu_seqlens=[0])) == H3GQA_OK

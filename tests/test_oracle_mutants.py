@@ -12,6 +12,7 @@ import pytest
 
 from oracle import causal_gqa as orc
 from tests import test_oracle_pins as pins
+from tests import test_oracle_prep_pins as prep_pins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "causal_gqa_oracle.c")
@@ -36,6 +37,16 @@ MUTANTS = [
      "q[((int64_t)g * T + i) * d + c]"),
     ("probabilities not normalised", "const double p = exp(z[jj] - L);",
      "const double p = exp(z[jj] - m);"),
+]
+
+PREP_MUTANTS = [
+    ("rotation pairs neighbours", "const double a = y[i], b = y[i + half];",
+     "const double a = y[i], b = y[(i + 1) % d];"),
+    ("rotation sign", "y[i] = a * cs - b * sn;", "y[i] = a * cs + b * sn;"),
+    ("norm weight dropped", "y[c] = y[c] * inv * bf16_bits_to_double(w[c]);",
+     "y[c] = y[c] * inv;"),
+    ("sum instead of mean", "ms /= d;", "ms /= 1;"),
+    ("eps dropped", "const double inv = 1.0 / sqrt(ms + eps);", "const double inv = 1.0 / sqrt(ms);"),
 ]
 
 PIN_CALLS = [
@@ -67,6 +78,30 @@ def _build_mutant(tmp_path, name, old, new):
     subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o",
                     str(lib), str(path_c), "-lm"], check=True)
     return str(lib)
+
+
+PREP_PIN_CALLS = [
+    ("rms-torch", prep_pins.test_rms_norm_matches_torch_float64),
+    ("unit-ms", prep_pins.test_unit_weight_gives_unit_mean_square_and_eps_shift),
+    ("scale-inv", prep_pins.test_norm_is_scale_invariant),
+    ("identity", prep_pins.test_identity_tables_leave_rows_unchanged),
+    ("pair-norms", prep_pins.test_rotation_keeps_pair_norms),
+    ("relative", prep_pins.test_rotated_dot_product_depends_on_position_difference),
+    ("angles-add", prep_pins.test_rotation_angles_add),
+]
+
+
+@pytest.mark.parametrize("name,old,new", PREP_MUTANTS, ids=[m[0] for m in PREP_MUTANTS])
+def test_prep_pins_catch_mutant(tmp_path, monkeypatch, name, old, new):
+    lib = orc.bind(_build_mutant(tmp_path, name, old, new))
+    monkeypatch.setattr(orc, "_LIB", lib)
+    caught = []
+    for pin_name, call in PREP_PIN_CALLS:
+        try:
+            call()
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(pin_name)
+    assert caught, "no pin caught the planted mistake: %s" % name
 
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
