@@ -72,38 +72,6 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
-// Register reallocation between warpgroups (all warps of a warpgroup run
-// the same instruction). The block's total never changes: what one
-// warpgroup gives back is what the others may take.
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_dec()
-{
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_inc()
-{
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-
-// Named barrier `id` over `count` threads (whole warps) that also returns
-// the OR of `pred` over all of them, so every participant takes the same
-// decision afterwards.
-__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy accesses (tensor core operand reads) to the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -271,26 +239,13 @@ __device__ __forceinline__ void tmem_st_wait()
 }
 
 // ------------------------------------------------------------- descriptors
-// Shared-memory matrix descriptor for tcgen05.mma with the 128-byte swizzle
-// (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B). Address and byte
-// offsets are encoded in 16-byte units; bits 46-47 hold the descriptor
-// version (1); bits 61-63 the layout (2 = 128-byte swizzle). The matrix base
-// must sit on a 1024-byte boundary (base-offset field left 0).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                uint32_t sbo_bytes)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
-
-// The same descriptor split in two 32-bit words: the low word carries the
-// start address and the leading byte offset, the high word the stride byte
-// offset, version and swizzle mode (a per-layout constant). Stepping a
+// Shared-memory matrix descriptor of tcgen05.mma for the 128-byte swizzle
+// (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B), built as two
+// 32-bit words. Low word: start address (bits 0-13, in 16-byte units) and
+// leading byte offset (bits 16-29, 16-byte units). High word: stride byte
+// offset (bits 32-45), descriptor version 1 (bits 46-47) and layout 2 =
+// 128-byte swizzle (bits 61-63); the base-offset field stays 0, so matrix
+// bases sit on 1024-byte boundaries. Stepping a
 // descriptor through a tile is then one 32-bit add on the low word (no
 // carry: shared-memory addresses stay below 256 KB, i.e. < 2^14 in 16-byte
 // units).
