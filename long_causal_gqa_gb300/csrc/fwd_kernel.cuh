@@ -53,7 +53,9 @@ constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + k
               kBarSFull = 2 + 2 * kStages, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2,
               kBarDrain = kBarOFull + 2, kBarQReady = kBarDrain + 2, kNumBars = kBarQReady + 2;
 constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag, [2..3] MMA turn counters
-constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kSchedOff = kMiscOff + 16;          // softmax threads' unit-schedule state, one slot each
+constexpr uint32_t kSchedSlotBytes = 24;
+constexpr uint32_t kSmemBytes = kSchedOff + 256 * kSchedSlotBytes + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if the max grew by > 2^8
 #ifndef H3GQA_WAIT_NS
@@ -92,9 +94,12 @@ struct FwdParams {
     int tile_tokens;        // 128 / G tokens per query tile
     int tile_tokens_log2;
     int unit_tokens;        // 2 * tile_tokens
+    int unit_tokens_log2;
     int blocks_per_class;   // 128 / unit_tokens: units of one sequence that visit the same number of K/V tiles
+    int blocks_per_class_log2;
     int n_seqs;             // non-empty sequences, sorted by length (descending)
     int c_max;              // most K/V tiles any unit visits
+    int full_windows;       // (n_units / n_kv_heads) / grid: whole windows of the unit schedule
     float scale_log2;       // scale * log2(e)
     int seq_start[kMaxSeqs];
     int seq_len[kMaxSeqs];
@@ -107,14 +112,17 @@ struct Unit {
     int kv_head;
 };
 
-// Walks the global longest-first unit order. Units are grouped by cost
-// class c (= K/V tiles visited, from c_max down to 1); inside a class by
-// sequence (longest first), then block, then KV head. Every role of a CTA
-// runs the same walk, so no schedule is stored anywhere.
+// Walks the global longest-first order of block slots (a slot is one token
+// block of one sequence; it becomes a unit once a KV head is attached).
+// Slots are grouped by cost class c (= K/V tiles visited, from c_max down to
+// 1); inside a class by sequence (longest first), then block. Without the
+// causal rule every slot of a sequence costs the same: longest sequence
+// first, then block. Every role of a CTA runs the same walk, so no schedule
+// is stored anywhere. Successive seeks must not go backwards.
 struct UnitWalker {
     int c;
     int i;
-    long long base;
+    int base;       // first slot of the current (class, sequence) group; slots fit in int
 
     __device__ __forceinline__ void init(const FwdParams &p)
     {
@@ -123,55 +131,58 @@ struct UnitWalker {
         base = 0;
     }
 
+    __device__ __forceinline__ int blocks_of(const FwdParams &p, int seq) const
+    {
+        return (p.seq_len[seq] + p.unit_tokens - 1) >> p.unit_tokens_log2;
+    }
+
     __device__ __forceinline__ int blocks_in_class(const FwdParams &p, int cls, int seq) const
     {
-        const int nblk = (p.seq_len[seq] + p.unit_tokens - 1) / p.unit_tokens;
-        const int lo = (cls - 1) * p.blocks_per_class;
-        const int hi = min(cls * p.blocks_per_class, nblk);
+        const int lo = (cls - 1) << p.blocks_per_class_log2;
+        const int hi = min(cls << p.blocks_per_class_log2, blocks_of(p, seq));
         return hi > lo ? hi - lo : 0;
     }
 
-    __device__ __forceinline__ int blocks_of(const FwdParams &p, int seq) const
+    // slot must not decrease from one call to the next, and slot < n_units / n_kv_heads.
+    __device__ __forceinline__ Unit seek(const FwdParams &p, int slot)
     {
-        return (p.seq_len[seq] + p.unit_tokens - 1) / p.unit_tokens;
-    }
-
-    // u must not decrease from one call to the next, and u < n_units.
-    __device__ __forceinline__ Unit seek(const FwdParams &p, long long u)
-    {
-        if (!p.causal) {
-            // Without the causal rule every unit of a sequence visits all of
-            // its key tiles: longest sequence first, then block, then KV head.
+        Unit r;
+        if (p.causal && p.n_seqs == 1) {
+            // One sequence: the top class holds the blocks past the last
+            // whole class, every lower class blocks_per_class of them.
+            const int nblk = blocks_of(p, 0);
+            const int top = nblk - ((p.c_max - 1) << p.blocks_per_class_log2);
+            if (slot < top) {
+                r.block = ((p.c_max - 1) << p.blocks_per_class_log2) + slot;
+            } else {
+                const int s2 = slot - top;
+                const int cls = p.c_max - 1 - (s2 >> p.blocks_per_class_log2);
+                r.block = ((cls - 1) << p.blocks_per_class_log2) + (s2 & (p.blocks_per_class - 1));
+            }
+        } else if (!p.causal) {
             for (;;) {
-                const long long cnt = (long long)blocks_of(p, i) * p.n_kv_heads;
-                if (u < base + cnt) break;
+                const int cnt = blocks_of(p, i);
+                if (slot < base + cnt) break;
                 base += cnt;
                 ++i;
             }
-            const long long j = u - base;
-            Unit r;
-            r.seq_start = p.seq_start[i];
-            r.seq_len = p.seq_len[i];
-            r.kv_head = (int)(j % p.n_kv_heads);
-            r.block = (int)(j / p.n_kv_heads);
-            return r;
-        }
-        for (;;) {
-            const long long cnt = (long long)blocks_in_class(p, c, i) * p.n_kv_heads;
-            if (u < base + cnt) break;
-            base += cnt;
-            ++i;
-            if (i >= p.n_seqs || blocks_in_class(p, c, i) == 0) {
-                i = 0;
-                --c;
+            r.block = slot - base;
+        } else {
+            for (;;) {
+                const int cnt = blocks_in_class(p, c, i);
+                if (slot < base + cnt) break;
+                base += cnt;
+                ++i;
+                if (i >= p.n_seqs || blocks_in_class(p, c, i) == 0) {
+                    i = 0;
+                    --c;
+                }
             }
+            r.block = ((c - 1) << p.blocks_per_class_log2) + (slot - base);
         }
-        const long long j = u - base;
-        Unit r;
         r.seq_start = p.seq_start[i];
         r.seq_len = p.seq_len[i];
-        r.kv_head = (int)(j % p.n_kv_heads);
-        r.block = (c - 1) * p.blocks_per_class + (int)(j / p.n_kv_heads);
+        r.kv_head = 0;
         return r;
     }
 };
@@ -183,15 +194,53 @@ __device__ __forceinline__ int unit_kv_tiles(const FwdParams &p, const Unit &un)
     return p.causal ? (un.block * p.unit_tokens) / kKeys + 1 : (un.seq_len + kKeys - 1) / kKeys;
 }
 
-// Round r of the static schedule hands CTA x the unit r*grid + x on even
-// rounds and r*grid + (grid-1-x) on odd ones (a snake over the longest-first
-// order), which evens out the linearly falling unit costs.
+// Round r of the static schedule hands CTA x the unit index r*grid + x on
+// even rounds and r*grid + (grid-1-x) on odd ones (a snake), which evens out
+// the falling unit costs of the longest-first order.
 __device__ __forceinline__ long long unit_of_round(long long r)
 {
     const long long g = gridDim.x;
     const long long x = blockIdx.x;
     return r * g + ((r & 1) ? (g - 1 - x) : x);
 }
+
+// Maps unit indices to (slot, KV head). The slot order is cut into windows of
+// grid slots; inside a window the KV head is the slowest index, so the grid's
+// CTAs, which run one round at a time, work on one KV head and share its K/V
+// tiles in L2 (with the head fastest, a round spans every head and a long
+// sequence's K/V no longer fits in L2). Round r of window r / Hkv runs head
+// r mod Hkv on slot x or grid-1-x; even and odd rounds keep a walker each, so
+// both only move forward. The last, partial window keeps the head fastest.
+struct Schedule {
+    UnitWalker even, odd;
+
+    __device__ __forceinline__ void init(const FwdParams &p)
+    {
+        even.init(p);
+        odd.init(p);
+    }
+
+    // The unit of round r (r < n_units < 2^31); r must not decrease between calls.
+    __device__ __forceinline__ Unit at(const FwdParams &p, long long r64)
+    {
+        const int r = (int)r64;
+        const int g = gridDim.x;
+        const int x = (r & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x;
+        const int w = r / p.n_kv_heads;
+        Unit un;
+        if (w < p.full_windows) {
+            un = ((r & 1) ? odd : even).seek(p, w * g + x);
+            un.kv_head = r - w * p.n_kv_heads;
+        } else {
+            const int q = (r - p.full_windows * p.n_kv_heads) * g + x;
+            const int qs = q / p.n_kv_heads;
+            un = even.seek(p, p.full_windows * g + qs);
+            un.kv_head = q - qs * p.n_kv_heads;
+        }
+        return un;
+    }
+};
+static_assert(sizeof(Schedule) == kSchedSlotBytes, "schedule slot size");
 
 __device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned int who)
@@ -288,7 +337,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             tma_prefetch_map(&p.map_q);
             tma_prefetch_map(&p.map_k);
             tma_prefetch_map(&p.map_v);
-            UnitWalker w;
+            Schedule w;
             w.init(p);
             uint32_t kv_it = 0, unit_it = 0;
             int last_kv_parity[kStages];
@@ -298,7 +347,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             for (long long r = 0; ok; ++r) {
                 const long long u = unit_of_round(r);
                 if (u >= p.n_units) break;
-                const Unit un = w.seek(p, u);
+                const Unit un = w.at(p, r);
                 const int tb = un.block * p.unit_tokens;
                 const int n_kv = unit_kv_tiles(p, un);
                 if (!wait_poll(bar(kBarQEmpty), (unit_it & 1) ^ 1, abort_flag, 1u)) { ok = false; break; }
@@ -361,7 +410,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             const uint32_t tS = tmem + (uint32_t)t * 128u;
             const uint32_t tO = tmem + 256u + (uint32_t)t * 128u;
             const uint32_t sQt = sQ + (uint32_t)t * kTileBytes;
-            UnitWalker w;
+            Schedule w;
             w.init(p);
             uint32_t kv_it = 0, unit_it = 0, p_phase = 0, turns = 0;
             bool ok = true;
@@ -427,7 +476,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             for (long long r = 0; ok; ++r) {
                 const long long u = unit_of_round(r);
                 if (u >= p.n_units) break;
-                const Unit un = w.seek(p, u);
+                const Unit un = w.at(p, r);
                 const int n_kv = unit_kv_tiles(p, un);
                 if (!wait_poll(bar(p.prep_q ? kBarQReady + t : kBarQFull), unit_it & 1, abort_flag, who)) {
                     ok = false;
@@ -571,15 +620,21 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             return true;
         };
 
-        UnitWalker w;
+        // The schedule state lives in this thread's shared-memory slot: it is
+        // used once per unit, and the registers are needed by the score rows.
+        Schedule &w = reinterpret_cast<Schedule *>(smem + kSchedOff)[threadIdx.x];
         w.init(p);
         uint32_t s_phase = 0, o_phase = 0, q_it = 0;
         bool ok = true;
-        if (p.prep_q && unit_of_round(0) < p.n_units) ok = prep_q(w.seek(p, unit_of_round(0)), 0);
+        // Each unit is looked up at the end of the one before, where the
+        // score rows are no longer live.
+        Unit un;
+        if (unit_of_round(0) < p.n_units) {
+            un = w.at(p, 0);
+            if (p.prep_q) ok = prep_q(un, 0);
+        }
         for (long long r = 0; ok; ++r) {
-            const long long u = unit_of_round(r);
-            if (u >= p.n_units) break;
-            const Unit un = w.seek(p, u);
+            if (unit_of_round(r) >= p.n_units) break;
             const int tb = un.block * p.unit_tokens;
             const int n_kv = unit_kv_tiles(p, un);
             const int tok = tb + t * p.tile_tokens + tok_in_tile;   // token inside its sequence
@@ -661,10 +716,11 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             // The next unit's Q tile lands while this unit's last P.V and the
             // epilogue run; its rotary table rows are pulled into L1 now.
             ++q_it;
-            const bool prep_next = p.prep_q && unit_of_round(r + 1) < p.n_units;
-            Unit next_un;
+            const bool has_next = unit_of_round(r + 1) < p.n_units;
+            const bool prep_next = p.prep_q && has_next;
+            Unit next_un = un;
             if (prep_next) {
-                next_un = w.seek(p, unit_of_round(r + 1));
+                next_un = w.at(p, r + 1);
                 if (p.rope_cos != nullptr && !p.stage_rope) {
                     const long long tn = (long long)next_un.seq_start + next_un.block * p.unit_tokens +
                                          t * p.tile_tokens + tok_in_tile;
@@ -743,6 +799,8 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             if (valid) p.lse[grow] = (m + __log2f(l)) * 0.69314718055994531f;
             tc_fence_before_sync();
             if (prep_next && !prep_q(next_un, q_it)) { ok = false; break; }
+            if (has_next && !prep_next) next_un = w.at(p, r + 1);
+            un = next_un;
         }
     }
 

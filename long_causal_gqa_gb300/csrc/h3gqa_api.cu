@@ -20,6 +20,7 @@ using h3gqa::FwdParams;
 
 constexpr int kVersion = 10000;   // 1.0.0
 constexpr long long kMaxTotalTokens = (1LL << 31) - 256;
+constexpr long long kMaxUnits = (1LL << 31) - 1;
 
 struct HostPlan {
     int group = 0;
@@ -86,6 +87,8 @@ h3gqa_status build_plan(const int32_t *cu, int n_seqs, int hq, int hkv, int head
             p.n_kv_tiles += nblk * ((len + h3gqa::kKeys - 1) / h3gqa::kKeys) * hkv;
         }
     }
+    // the kernel counts units and rounds in 32-bit integers
+    if (p.n_units > kMaxUnits) return H3GQA_ERR_UNSUPPORTED;
     if (!p.len.empty()) {
         const long long nblk0 = (p.len[0] + p.unit_tokens - 1) / p.unit_tokens;
         p.c_max = causal ? (int)((nblk0 + p.blocks_per_class - 1) / p.blocks_per_class)
@@ -304,7 +307,9 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
     prm->tile_tokens = hp.tile_tokens;
     prm->tile_tokens_log2 = ilog2(hp.tile_tokens);
     prm->unit_tokens = hp.unit_tokens;
+    prm->unit_tokens_log2 = ilog2(hp.unit_tokens);
     prm->blocks_per_class = hp.blocks_per_class;
+    prm->blocks_per_class_log2 = ilog2(hp.blocks_per_class);
     prm->n_seqs = (int)hp.len.size();
     prm->c_max = hp.c_max;
     prm->scale_log2 = scale * 1.4426950408889634f;
@@ -313,6 +318,7 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
         prm->seq_len[i] = hp.len[i];
     }
     const long long grid = std::min<long long>(hp.n_units, ds->sm_count);
+    prm->full_windows = (int)(hp.n_units / n_kv_heads / grid);
     h3gqa::causal_gqa_fwd_kernel<<<(unsigned)grid, h3gqa::kThreads, h3gqa::kSmemBytes,
                                    reinterpret_cast<cudaStream_t>(stream)>>>(*prm);
     delete prm;
