@@ -46,7 +46,11 @@ constexpr uint32_t kKvOff = kQOff + 2 * kTileBytes;
 constexpr uint32_t kRopeOff = kKvOff + kStages * kTileBytes;   // cos rows, then sin rows, of one unit
 constexpr uint32_t kRopeRowBytes = kHeadDim / 2 * 4;           // 64 fp32 per token
 constexpr int kRopeMaxTokens = 32;                             // staged when a unit has <= 32 tokens (G >= 8)
-constexpr uint32_t kRopeBytes = 2 * kRopeMaxTokens * kRopeRowBytes;
+// Staged rows are 16 bytes apart beyond their length, so the eight tokens a
+// quarter-warp reads at one column fall in eight different bank groups (with
+// a 256-byte stride they would all hit the same four banks).
+constexpr uint32_t kRopeStride = kRopeRowBytes + 16;
+constexpr uint32_t kRopeBytes = 2 * kRopeMaxTokens * kRopeStride;
 constexpr uint32_t kBarOff = kRopeOff + kRopeBytes;
 // barrier slots
 constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + kStages,
@@ -359,10 +363,13 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 }
                 mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes + 2 * rope_bytes);
                 last_q_parity = unit_it & 1;
-                if (rope_bytes != 0) {
-                    bulk_load(sbase + kRopeOff, p.rope_cos + tok0 * (kHeadDim / 2), rope_bytes, bar(kBarQFull));
-                    bulk_load(sbase + kRopeOff + kRopeBytes / 2, p.rope_sin + tok0 * (kHeadDim / 2), rope_bytes,
+                // one copy per token row (cos, then sin), into the padded rows
+                for (uint32_t rr = 0; rr < rope_bytes / kRopeRowBytes; ++rr) {
+                    const long long tr = tok0 + rr;
+                    bulk_load(sbase + kRopeOff + rr * kRopeStride, p.rope_cos + tr * (kHeadDim / 2), kRopeRowBytes,
                               bar(kBarQFull));
+                    bulk_load(sbase + kRopeOff + kRopeBytes / 2 + rr * kRopeStride, p.rope_sin + tr * (kHeadDim / 2),
+                              kRopeRowBytes, bar(kBarQFull));
                 }
                 for (int t = 0; t < 2; ++t)
                     for (int h = 0; h < 2; ++h)
@@ -592,7 +599,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                         float4 c0, c1, s0, s1;
                         if (p.stage_rope) {
                             const float4 *cs4 = reinterpret_cast<const float4 *>(
-                                smem + kRopeOff + (uint32_t)(t * p.tile_tokens + tok_in_tile) * kRopeRowBytes) + 2 * cc;
+                                smem + kRopeOff + (uint32_t)(t * p.tile_tokens + tok_in_tile) * kRopeStride) + 2 * cc;
                             const float4 *sn4 = cs4 + kRopeBytes / 2 / 16;
                             c0 = cs4[0]; c1 = cs4[1]; s0 = sn4[0]; s1 = sn4[1];
                         } else {
