@@ -110,14 +110,17 @@ struct DeviceState {
     int sm_count = 0;
 };
 
+// A fixed table, so a DeviceState handed out stays where it is while other
+// threads set up other devices.
+constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-std::vector<DeviceState> g_devices;
+DeviceState g_devices[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
 
 h3gqa_status device_setup(int dev, DeviceState **out)
 {
+    if (dev < 0 || dev >= kMaxDevices) return H3GQA_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if ((int)g_devices.size() <= dev) g_devices.resize(dev + 1);
     DeviceState &d = g_devices[dev];
     if (d.ready) {
         *out = &d;
