@@ -1,0 +1,74 @@
+"""The library is reentrant: host threads that call it at the same time, each
+on its own stream with its own buffers, get exactly the results of calls made
+one after another (the kernel has no atomics and no shared scratch, so the
+outputs are bitwise reproducible)."""
+import threading
+
+import pytest
+import torch
+
+from long_causal_gqa_gb300 import binding
+from long_causal_gqa_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+SCALE = 128 ** -0.5
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    binding.load()
+    return torch.device("cuda:0")
+
+
+def test_threads_on_separate_streams(dev):
+    jobs = [dict(seqlens=(1500, 0, 333), causal=True, token_major=False, seed=71),
+            dict(seqlens=(2049,), causal=False, token_major=True, seed=72),
+            dict(seqlens=(640, 77, 1), causal=True, token_major=True, seed=73)]
+    inputs = []
+    for j in jobs:
+        x = make_inputs(j["seqlens"], 64, 8, 128, j["seed"])
+        inputs.append((x, tuple(x[n].to(dev) for n in ("q", "k", "v"))))
+    # one after another on the default stream
+    expected = []
+    for j, (x, (q, k, v)) in zip(jobs, inputs):
+        o, lse, _ = binding.attention_fwd(q, k, v, x["cu_seqlens"], SCALE, causal=j["causal"],
+                                          token_major=j["token_major"])
+        binding.h3gqa_sync_and_check(torch.cuda.current_stream(dev).cuda_stream)
+        expected.append((o.clone(), lse.clone()))
+
+    results = [None] * len(jobs)
+    errors = []
+    start = threading.Barrier(len(jobs))
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(dev)
+            j, (x, (q, k, v)) = jobs[i], inputs[i]
+            stream = torch.cuda.Stream(dev)
+            outs = []
+            start.wait()
+            with torch.cuda.stream(stream):
+                for _ in range(4):
+                    o, lse, _ = binding.attention_fwd(q, k, v, x["cu_seqlens"], SCALE,
+                                                      causal=j["causal"],
+                                                      token_major=j["token_major"],
+                                                      stream=stream)
+                    outs.append((o, lse))
+            binding.h3gqa_sync_and_check(stream.cuda_stream)
+            results[i] = outs
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(jobs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not errors, errors
+    for i, outs in enumerate(results):
+        assert outs is not None
+        for o, lse in outs:
+            assert torch.equal(o, expected[i][0]) and torch.equal(lse, expected[i][1]), \
+                "job %d differs from its sequential result" % i
