@@ -25,15 +25,17 @@
  *   lse  : [n_q_heads][T] fp32 (natural log)
  *
  * Ownership and threading. The caller owns every buffer. Calls allocate no
- * device memory and keep no per-call state. Work is queued on `stream` and
- * the call returns without waiting for it. Calls on different streams may
- * run concurrently as long as their outputs do not overlap.
+ * device memory and keep no per-call state. Work is queued on `stream`, on
+ * the calling thread's current CUDA device (ordinals 0-63), and the call
+ * returns without waiting for it. Any number of host threads may call the
+ * library at once; calls on different streams may run concurrently as long
+ * as their outputs do not overlap.
  *
  * Errors. Every entry point returns a status and never exits or aborts the
  * process. Argument checks run on the host before any CUDA call. A kernel
- * whose internal pipeline waits exceed their iteration bound stops, frees
- * what it holds and raises a device-side flag; h3gqa_sync_and_check reports
- * it as H3GQA_ERR_TIMEOUT.
+ * whose internal pipeline wait exceeds its time bound (2 s of wall clock)
+ * stops, lets its in-flight copies finish, frees what it holds and raises a
+ * device-side flag; h3gqa_sync_and_check reports it as H3GQA_ERR_TIMEOUT.
  */
 #ifndef H3GQA_H_
 #define H3GQA_H_
@@ -50,7 +52,7 @@ typedef struct CUstream_st *h3gqa_stream_t;
 typedef enum {
     H3GQA_OK = 0,
     H3GQA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad cu_seqlens, bad scale, heads */
-    H3GQA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim != 128, group size, too many sequences */
+    H3GQA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim != 128, group size, too many sequences, device ordinal >= 64 */
     H3GQA_ERR_ARCH = 3,          /* current device is not compute capability 10.3 */
     H3GQA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     H3GQA_ERR_TIMEOUT = 5        /* a kernel gave up on a bounded internal wait */
