@@ -578,7 +578,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 }
                 // element i of the first half pairs with element i + 64 for the
                 // rotation, so chunk cc of both halves is processed together
-#pragma unroll 2
+#pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
                     float a[8], b[8];
                     unpack(*chunk(0, cc), a);
