@@ -104,6 +104,9 @@ def load(path: str = LIB_PATH):
 
 def _cu_array(cu_seqlens):
     vals = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    # ctypes would wrap values outside int32 silently; the C ABI takes int32
+    if any(v < -2 ** 31 or v >= 2 ** 31 for v in vals):
+        raise ValueError("cu_seqlens values must fit in int32")
     arr = (ctypes.c_int32 * max(len(vals), 1))(*vals)
     return arr, len(vals) - 1
 

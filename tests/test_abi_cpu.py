@@ -200,3 +200,8 @@ def test_prologue_options_rejected_before_cuda(lib):
                               k_out_ptr=good)
     assert binding.h3gqa_attention_fwd(options=ok, check=False,
                                        **dict(base, cu_seqlens=[0])) == H3GQA_OK
+
+
+def test_cu_seqlens_outside_int32_rejected_in_the_binding(lib):
+    with pytest.raises(ValueError):
+        binding.h3gqa_make_plan([0, 2 ** 31], 64, 8)
