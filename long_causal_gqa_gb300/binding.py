@@ -183,6 +183,50 @@ def h3gqa_sync_and_check(stream=0, check=True):
     return st
 
 
+def _cu_total(cu_seqlens):
+    vals = cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else list(cu_seqlens)
+    if len(vals) == 0:
+        raise ValueError("cu_seqlens needs at least one entry")
+    return int(vals[-1])
+
+
+def check_tensors(q, k, v, cu_seqlens, q_norm_weight=None, k_norm_weight=None, rope_cos=None,
+                  rope_sin=None, k_out=None, o=None, lse=None, o_shape=None):
+    """Shape, dtype and layout checks of the torch front ends. The C ABI takes
+    raw pointers and cannot see sizes, so a short table or output here would
+    be read or written out of bounds on the device; these checks run first."""
+    import torch
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be [heads, T, head_dim]")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bf16 tensor" % name)
+    hq, T, d = q.shape
+    hkv = k.shape[0]
+    if k.shape != (hkv, T, d) or v.shape != (hkv, T, d):
+        raise ValueError("k and v must be [Hkv, T, D] with q's T and D")
+    if _cu_total(cu_seqlens) != T:
+        raise ValueError("cu_seqlens[-1] must equal T = q.shape[1]")
+    for name, t, shape, dtype in (("q_norm_weight", q_norm_weight, (d,), torch.bfloat16),
+                                  ("k_norm_weight", k_norm_weight, (d,), torch.bfloat16),
+                                  ("rope_cos", rope_cos, (T, d // 2), torch.float32),
+                                  ("rope_sin", rope_sin, (T, d // 2), torch.float32),
+                                  ("k_out", k_out, tuple(k.shape), torch.bfloat16),
+                                  ("lse", lse, (hq, T), torch.float32)):
+        if t is not None and (tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous()):
+            raise ValueError("%s must be a contiguous %s tensor of shape %s" % (name, dtype, shape))
+    if o is not None and (tuple(o.shape) != tuple(o_shape or q.shape) or
+                          o.dtype != torch.bfloat16 or not o.is_contiguous()):
+        raise ValueError("o must be a contiguous bf16 tensor shaped like q")
+    return hq, hkv, T, d
+
+
+def _check_cuda(*tensors):
+    for t in tensors:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+
+
 def attention_fwd(q, k, v, cu_seqlens, scale=None, causal=True, token_major=False,
                   out_int8=False, stream=None, q_norm_weight=None, k_norm_weight=None,
                   rope_cos=None, rope_sin=None, norm_eps=1e-6, k_out=None):
@@ -193,13 +237,9 @@ def attention_fwd(q, k, v, cu_seqlens, scale=None, causal=True, token_major=Fals
     the prepared keys go to k_out (allocated if not given; read it back as
     the post-prologue key cache)."""
     import torch
-    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
-        raise ValueError("q, k, v must be [heads, T, head_dim]")
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError("%s must be a contiguous bf16 CUDA tensor" % name)
-    hq, T, d = q.shape
-    hkv = k.shape[0]
+    hq, hkv, T, d = check_tensors(q, k, v, cu_seqlens, q_norm_weight, k_norm_weight, rope_cos,
+                                  rope_sin, k_out)
+    _check_cuda(q, k, v, q_norm_weight, k_norm_weight, rope_cos, rope_sin, k_out)
     if scale is None:
         scale = d ** -0.5
     shape = (T, hq, d) if token_major else (hq, T, d)
@@ -212,10 +252,6 @@ def attention_fwd(q, k, v, cu_seqlens, scale=None, causal=True, token_major=Fals
     if prep_k and k_out is None:
         k_out = torch.empty_like(k)
     ptr = lambda t: t.data_ptr() if t is not None else None
-    for name, t in (("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight),
-                    ("rope_cos", rope_cos), ("rope_sin", rope_sin)):
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
-            raise ValueError("%s must be a contiguous CUDA tensor" % name)
     opts = make_options(causal, H3GQA_LAYOUT_TOKEN_MAJOR if token_major else
                         H3GQA_LAYOUT_HEAD_MAJOR, out_int8, ptr(o_scale), 0, ptr(q_norm_weight),
                         ptr(k_norm_weight), ptr(rope_cos), ptr(rope_sin),
@@ -232,15 +268,8 @@ def causal_gqa_fwd(q, k, v, cu_seqlens, scale=None, o=None, lse=None, stream=Non
     cu_seqlens host ints. Returns (o [Hq,T,D] bf16, lse [Hq,T] fp32) on q's device,
     queued on `stream` (default: torch's current stream)."""
     import torch
-    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
-        raise ValueError("q, k, v must be [heads, T, head_dim]")
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError("%s must be a contiguous bf16 CUDA tensor" % name)
-    hq, T, d = q.shape
-    hkv = k.shape[0]
-    if k.shape != (hkv, T, d) or v.shape != (hkv, T, d):
-        raise ValueError("k and v must be [Hkv, T, D] with q's T and D")
+    hq, hkv, T, d = check_tensors(q, k, v, cu_seqlens, o=o, lse=lse)
+    _check_cuda(q, k, v, o, lse)
     if scale is None:
         scale = d ** -0.5
     if o is None:

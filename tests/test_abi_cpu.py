@@ -22,7 +22,8 @@ def lib():
 
 
 def _declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as fh:
+        text = fh.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(h3gqa_[a-z_0-9]+)\s*\(", text)))
 
@@ -141,8 +142,9 @@ def test_library_links_no_oracle():
     for dirpath, _, files in os.walk(src_dir):
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h")):
-                assert "oracle" not in open(os.path.join(dirpath, f)).read().lower() or \
-                    f == "inputs.py", f
+                with open(os.path.join(dirpath, f)) as fh:
+                    text = fh.read().lower()
+                assert "oracle" not in text or f == "inputs.py", f
 
 
 def test_attention_plan_bidirectional(lib):
@@ -205,3 +207,31 @@ def test_prologue_options_rejected_before_cuda(lib):
 def test_cu_seqlens_outside_int32_rejected_in_the_binding(lib):
     with pytest.raises(ValueError):
         binding.h3gqa_make_plan([0, 2 ** 31], 64, 8)
+
+
+def test_front_end_shape_checks_on_cpu_tensors():
+    import torch
+    T, d = 40, 128
+    q = torch.zeros(8, T, d, dtype=torch.bfloat16)
+    k = torch.zeros(2, T, d, dtype=torch.bfloat16)
+    v = torch.zeros(2, T, d, dtype=torch.bfloat16)
+    assert binding.check_tensors(q, k, v, [0, 30, T]) == (8, 2, T, d)
+    bad = [
+        dict(cu_seqlens=[0, T - 1]),                                         # T mismatch
+        dict(k=torch.zeros(2, T + 1, d, dtype=torch.bfloat16)),              # k's T
+        dict(v=torch.zeros(2, T, d, dtype=torch.float16)),                   # dtype
+        dict(q=torch.zeros(8, d, T, dtype=torch.bfloat16).transpose(1, 2)),  # not contiguous
+        dict(rope_cos=torch.zeros(T - 1, d // 2)),                           # table too short
+        dict(rope_sin=torch.zeros(T, d // 2, dtype=torch.float64)),
+        dict(q_norm_weight=torch.zeros(d, dtype=torch.float32)),
+        dict(k_out=torch.zeros(2, T, d // 2, dtype=torch.bfloat16)),
+        dict(o=torch.zeros(8, T, d + 1, dtype=torch.bfloat16)),
+        dict(lse=torch.zeros(8, T + 1)),
+    ]
+    for b in bad:
+        args = dict(q=q, k=k, v=v, cu_seqlens=[0, T])
+        args.update(b)
+        with pytest.raises(ValueError):
+            binding.check_tensors(**args)
+    with pytest.raises(ValueError):
+        binding.attention_fwd(q, k, v, [0, T])          # CPU tensors never reach the library

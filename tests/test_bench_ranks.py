@@ -32,7 +32,7 @@ def _worker(rank, world, port, out):
 
 def test_two_ranks_take_the_slowest_time():
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()
     out = manager.dict()
     mp.start_processes(_worker, args=(2, port, out), nprocs=2, join=True, start_method="spawn")
     assert out[0] == out[1]

@@ -70,7 +70,8 @@ PIN_CALLS = [
 
 
 def _build_mutant(tmp_path, name, old, new):
-    src = open(SRC).read()
+    with open(SRC) as fh:
+        src = fh.read()
     assert src.count(old) == 1, "mutation site not found once: %r" % old
     path_c = tmp_path / "mutant.c"
     path_c.write_text(src.replace(old, new))

@@ -9,12 +9,13 @@ GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
 
 def _failing_lengths():
     out = []
-    for line in open(GOLDEN):
-        if line.startswith("#") or "|" not in line:
-            continue
-        cells = [c.strip() for c in line.split("|")]
-        if cells[2] == "fail":
-            out.append(int(cells[3]))
+    with open(GOLDEN) as fh:
+        for line in fh:
+            if line.startswith("#") or "|" not in line:
+                continue
+            cells = [c.strip() for c in line.split("|")]
+            if cells[2] == "fail":
+                out.append(int(cells[3]))
     return out
 
 
