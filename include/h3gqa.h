@@ -17,9 +17,9 @@
  *     o[h,i,:] = sum_j softmax_j(z) * v[g,j,:]
  *     lse[h,i] = ln sum_j exp(z_j)
  *
- * Layouts (all contiguous, head-major, the "[head,row,dimension]" attention
- * order that the h3.c README gives in its "Profiling and diagnostic paths"
- * section):
+ * Layouts (all contiguous and head-major: head, then row, then dimension,
+ * the attention order that the h3.c README describes in its "Profiling and
+ * diagnostic paths" section):
  *   q, o : [n_q_heads][T][head_dim] bf16     T = cu_seqlens[n_seqs]
  *   k, v : [n_kv_heads][T][head_dim] bf16
  *   lse  : [n_q_heads][T] fp32 (natural log)
@@ -98,7 +98,7 @@ h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v,
  *
  * out_layout = H3GQA_LAYOUT_TOKEN_MAJOR writes o as [T][Hq][head_dim], the
  * row-major order the out-projection reads, instead of leaving it in
- * [head,row,dimension] order for a separate gather (h3.c README, "Profiling
+ * head-major order for a separate gather (h3.c README, "Profiling
  * and diagnostic paths", which gathers and int8-quantizes the SDPA output on
  * its way into the out-projection).
  *

@@ -5,9 +5,9 @@
 // per call (every K tile is read by many units, so transforming it on each
 // load would repeat the work), writing the prepared keys the caller keeps.
 //
-// The step is the "fused QK-normalization/RoPE" that precedes attention in
-// the h3.c README ("Profiling and diagnostic paths", "Checkpoint layout and
-// media pipeline"):
+// The step is the fused Q/K normalisation and rotary embedding that the h3.c
+// README places before attention ("Profiling and diagnostic paths",
+// "Checkpoint layout and media pipeline"):
 //   y = x * rsqrt(mean(x^2) + eps) * w                       (if w given)
 //   for i < 64: (y_i, y_{i+64}) <- (y_i c - y_{i+64} s, y_{i+64} c + y_i s),
 //   c = cos[t][i], s = sin[t][i]                             (if tables given)
