@@ -192,6 +192,25 @@ def test_long_sequence_65536_sampled(dev):
     assert all_finite(o_t, lse_t)
 
 
+def test_long_sequence_262144_sampled(dev):
+    """A single 262144-token sequence (Hq 8, Hkv 4: 128-token units, up to
+    2048 K/V tiles per unit): no length bound, sampled rows across the whole
+    sequence, the last row of every head, and every output finite."""
+    S, hq, hkv = 262144, 8, 4
+    x = make_inputs((S,), hq, hkv, 128, seed=262144)
+    o_t, lse_t = run_gpu(x, hq, hkv, 128 ** -0.5, dev, as_numpy=False)
+    cu = x["cu_seqlens"].numpy()
+    rng = np.random.default_rng(11)
+    rows = np.stack([rng.integers(0, hq, 48), rng.integers(0, S, 48)], axis=1)
+    rows = np.concatenate([rows, np.array([[h, S - 1] for h in range(hq)] +
+                                          [[0, 0], [hq - 1, 127], [1, 128], [2, 131071]],
+                                          dtype=np.int64)])
+    ref_o, ref_lse = orc.causal_gqa_rows(x["q"], x["k"], x["v"], cu, hq, hkv, 128 ** -0.5, rows)
+    got_o, got_l = rows_of(o_t, lse_t, rows)
+    assert_close(got_o, got_l, ref_o, ref_lse, "S=262144")
+    assert all_finite(o_t, lse_t)
+
+
 def test_many_sequences_at_the_limit(dev):
     """1024 non-empty sequences (the most one call accepts) of random lengths,
     interleaved with empty ones; every row checked against the oracle."""
