@@ -72,3 +72,28 @@ def test_threads_on_separate_streams(dev):
         for o, lse in outs:
             assert torch.equal(o, expected[i][0]) and torch.equal(lse, expected[i][1]), \
                 "job %d differs from its sequential result" % i
+
+
+def test_cuda_graph_capture_and_replay(dev):
+    """A call captured in a CUDA graph replays to the eager result bit for bit
+    (the first, eager call does the per-device setup, which is not a stream
+    operation; the captured call only records the kernel launches)."""
+    x = make_inputs((3000, 0, 517), 64, 8, 128, seed=81)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o_ref, lse_ref, _ = binding.attention_fwd(q, k, v, x["cu_seqlens"], SCALE)
+    binding.h3gqa_sync_and_check(torch.cuda.current_stream(dev).cuda_stream)
+    o = torch.empty_like(o_ref)
+    lse = torch.empty_like(lse_ref)
+    stream = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        binding.h3gqa_causal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), x["cu_seqlens"], 64, 8, 128, SCALE,
+                                 torch.cuda.current_stream(dev).cuda_stream)
+    for _ in range(3):
+        o.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        assert binding.h3gqa_sync_and_check(0) == binding.H3GQA_OK
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
