@@ -29,7 +29,10 @@
  * the calling thread's current CUDA device (ordinals 0-63), and the call
  * returns without waiting for it. Any number of host threads may call the
  * library at once; calls on different streams may run concurrently as long
- * as their outputs do not overlap.
+ * as their outputs do not overlap. The first call on a device also does a
+ * one-time setup that is not a stream operation (kernel attributes, the
+ * driver's tensor-map entry point); after one such call, calls can be
+ * captured into CUDA graphs and replayed.
  *
  * Errors. Every entry point returns a status and never exits or aborts the
  * process. Argument checks run on the host before any CUDA call. A kernel
