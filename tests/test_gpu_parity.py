@@ -127,6 +127,24 @@ def test_large_scale_and_outliers_small(dev):
     full_check((700,), 64, 8, 32, dev, n_outlier=4)
 
 
+def test_extreme_logits_exercise_the_rescale(dev):
+    """q and k scaled by 6 (logit std ~36, rows nearly one-hot): the running
+    max jumps by far more than 2^8 many times per row, so the O rescale path
+    runs on many tiles; causal and bidirectional, checked in full."""
+    for causal in (True, False):
+        x = make_inputs((900, 0, 301), 64, 8, 128, seed=606)
+        x["q"] = (x["q"].float() * 6.0).to(torch.bfloat16)
+        x["k"] = (x["k"].float() * 6.0).to(torch.bfloat16)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        o, lse, _ = binding.attention_fwd(q, k, v, x["cu_seqlens"], 128 ** -0.5, causal=causal)
+        binding.h3gqa_sync_and_check(torch.cuda.current_stream(dev).cuda_stream)
+        ref_o, ref_lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], 64, 8,
+                                        128 ** -0.5, causal=causal)
+        assert_close(o.float().cpu().numpy().astype(np.float64),
+                     lse.cpu().numpy().astype(np.float64), ref_o, ref_lse,
+                     "extreme logits causal=%s" % causal)
+
+
 def test_deterministic_and_stream(dev):
     x = make_inputs((1000, 333), 64, 8, 128, seed=8)
     o1, l1 = run_gpu(x, 64, 8, 128 ** -0.5, dev)
