@@ -34,11 +34,24 @@
  * driver's tensor-map entry point); after one such call, calls can be
  * captured into CUDA graphs and replayed.
  *
+ * A device reset (cudaDeviceReset) drops the kernel attribute the setup
+ * made; a launch that fails for that reason sets the device up again and is
+ * retried once.
+ *
  * Errors. Every entry point returns a status and never exits or aborts the
  * process. Argument checks run on the host before any CUDA call. A kernel
  * whose internal pipeline wait exceeds its time bound (2 s of wall clock)
  * stops, lets its in-flight copies finish, frees what it holds and raises a
  * device-side flag; h3gqa_sync_and_check reports it as H3GQA_ERR_TIMEOUT.
+ * Rows of o and lse that such a kernel did not reach are left as they were.
+ * The flag is one word per device shared by every call on it; for a result
+ * that belongs to one call, pass h3gqa_options.status.
+ *
+ * Inputs must be finite. Keys a query must not see (later keys of its own
+ * sequence, keys of the next packed sequence in the same 128-key tile) get
+ * probability 0, but their value rows still enter the P.V product as 0 * v,
+ * so an infinite or NaN value anywhere in v[g][0..T) can reach rows that do
+ * not attend to it.
  */
 #ifndef H3GQA_H_
 #define H3GQA_H_
@@ -54,8 +67,8 @@ typedef struct CUstream_st *h3gqa_stream_t;
 
 typedef enum {
     H3GQA_OK = 0,
-    H3GQA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad cu_seqlens, bad scale, heads */
-    H3GQA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim != 128, group size, too many sequences, device ordinal >= 64 */
+    H3GQA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad cu_seqlens, bad scale, heads, options */
+    H3GQA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim != 128, too many sequences, T, device ordinal >= 64 */
     H3GQA_ERR_ARCH = 3,          /* current device is not compute capability 10.3 */
     H3GQA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     H3GQA_ERR_TIMEOUT = 5        /* a kernel gave up on a bounded internal wait */
@@ -71,8 +84,13 @@ typedef enum {
  *               cu[n_seqs] = T. Zero-length sequences are allowed. A single
  *               sequence of length S is {0, S}.
  *   n_seqs      number of packed sequences (>= 0; at most 1024 non-empty).
- *   n_q_heads, n_kv_heads   n_q_heads = G * n_kv_heads with G a power of two,
- *               2 <= G <= 128 (query head h reads KV head h / G).
+ *   n_q_heads, n_kv_heads   n_q_heads = G * n_kv_heads for any G >= 1
+ *               (query head h reads KV head h / G; G = 1 is plain multi-head
+ *               attention). Each 128-row MMA tile packs the query heads of
+ *               one KV head: all G of them when G <= 128 (else the largest
+ *               divisor of G that is <= 128) times floor(128 / heads) tokens,
+ *               so when 128 is not a multiple of G a few of its rows go
+ *               unused.
  *   head_dim    must be 128.
  *   scale       multiplies the logits; finite and > 0 (e.g. 1/sqrt(128)).
  *   stream      stream to queue the kernel on.
@@ -120,7 +138,7 @@ typedef struct {
     int32_t causal;        /* 1: key j visible to query i iff j <= i; 0: every key of the sequence */
     int32_t out_layout;    /* h3gqa_layout of o (and of o_scale) */
     int32_t out_int8;      /* 0: o is bf16; 1: o is int8 codes plus o_scale */
-    int32_t reserved;      /* must be 0 */
+    int32_t kv_head_begin; /* head shard: first KV head this call computes (0 = the first) */
     float *o_scale;        /* device fp32 [Hq][T] or [T][Hq], 4-byte aligned; required iff out_int8 */
     /* Q/K prologue (see below); all null = inputs are used as given. */
     const void *q_norm_weight;   /* device bf16 [head_dim], 16-byte aligned, or null */
@@ -128,10 +146,27 @@ typedef struct {
     const float *rope_cos;       /* device fp32 [T][head_dim/2], 16-byte aligned, or null */
     const float *rope_sin;       /* same shape; given together with rope_cos */
     void *k_out;                 /* device bf16 [Hkv][T][head_dim], 16-byte aligned: receives the
-                                    prepared keys; required iff k is prepared; may equal k */
+                                    prepared keys; required iff k is prepared; may equal k (then
+                                    k is overwritten, and a second such call prepares it again),
+                                    must not overlap q, v or part of k */
     float norm_eps;              /* added to the mean square; finite and >= 0 */
-    int32_t reserved2;           /* must be 0 */
+    int32_t kv_head_count;       /* head shard: KV heads this call computes; 0 = all from kv_head_begin */
+    uint32_t *status;            /* optional device word, 4-byte aligned, zeroed by the caller: a
+                                    kernel of this call that gives up on a bounded wait ORs a
+                                    non-zero bit into it (read it once the stream has finished) */
 } h3gqa_options;
+
+/*
+ * Head shard (kv_head_begin, kv_head_count). The KV heads, and with them
+ * their query heads, are independent: a call may compute only KV heads
+ * [kv_head_begin, kv_head_begin + kv_head_count) and the query heads that
+ * read them, so that several calls (on one GPU or one per GPU) together
+ * cover all heads with no exchange between them. Such a call writes only its
+ * heads' rows of o, lse and o_scale (the buffers keep their full shapes) and
+ * prepares only its heads' rows of k_out; every other row is left as it
+ * was. 0 <= kv_head_begin < n_kv_heads and kv_head_begin + kv_head_count <=
+ * n_kv_heads, else H3GQA_ERR_INVALID_ARG. The default (0, 0) is every head.
+ */
 
 /*
  * Q/K prologue (h3.c README, "Profiling and diagnostic paths" and
@@ -153,8 +188,10 @@ typedef struct {
  * i.e. exactly h3gqa_causal_fwd). Arguments and errors as for
  * h3gqa_causal_fwd; in addition an options value outside the ranges above,
  * out_int8 without a valid o_scale, a misaligned prologue pointer, rope_cos
- * without rope_sin (or the reverse) or a prepared k without k_out returns
- * H3GQA_ERR_INVALID_ARG. lse is always [Hq][T].
+ * without rope_sin (or the reverse), a prepared k without k_out, a k_out
+ * that overlaps q, v or part of k, a misaligned status word or a head shard
+ * outside [0, n_kv_heads) returns H3GQA_ERR_INVALID_ARG. lse is always
+ * [Hq][T].
  */
 h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v,
                                  void *o, float *lse,
@@ -164,9 +201,10 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v,
                                  h3gqa_stream_t stream);
 
 /* Work plan of one h3gqa_causal_fwd call, computed on the host only (no GPU
- * needed). A unit is (sequence, block of 256/G tokens, KV head); it owns two
- * 128-row query tiles (G heads x 128/G tokens each) and visits every 128-key
- * tile at or before its last token. */
+ * needed). A unit is (sequence, block of 2 * floor(128 / heads_per_tile)
+ * tokens, head group of heads_per_tile query heads); it owns two 128-row
+ * query tiles (heads_per_tile heads x floor(128 / heads_per_tile) tokens
+ * each) and visits every 128-key tile up to its last token. */
 typedef struct {
     int64_t total_tokens;       /* T */
     int64_t n_units;            /* work units */
@@ -176,8 +214,10 @@ typedef struct {
     double metric_flops;        /* headline count: causal sum_b 2*Hq*D*S_b^2 */
     double exp2_count;          /* needed exponentials, one per visible pair: causal sum_b Hq*S_b*(S_b+1)/2 */
     double algorithmic_bytes;   /* q,k,v read once + o,lse written once */
-    int32_t tokens_per_unit;    /* 256 / G */
+    int32_t tokens_per_unit;    /* 2 * floor(128 / heads_per_tile) (256 / G for G a power of two) */
     int32_t max_kv_tiles;       /* most 128-key tiles any unit visits */
+    int32_t heads_per_tile;     /* query heads packed in one tile: G if G <= 128 */
+    int32_t rows_per_tile;      /* used MMA rows of a tile (128 when G divides 128) */
 } h3gqa_plan;
 
 /* Fills *plan for the given shape; same argument rules as h3gqa_causal_fwd
@@ -197,7 +237,11 @@ h3gqa_status h3gqa_attention_plan(const int32_t *cu_seqlens, int n_seqs,
 /* Waits for `stream`, then reads and clears the current device's timeout
  * flag. Returns H3GQA_ERR_TIMEOUT if any kernel of this library on this
  * device gave up on a bounded wait since the last check, H3GQA_ERR_CUDA if
- * the synchronisation failed, else H3GQA_OK. */
+ * the synchronisation failed, else H3GQA_OK. The flag is device-wide: the
+ * timeout may belong to a call on another stream, and when two threads check
+ * the same device at once the read and the clear of one may straddle the
+ * other's, so one of them can miss a timeout. h3gqa_options.status gives
+ * each call its own word instead. */
 h3gqa_status h3gqa_sync_and_check(h3gqa_stream_t stream);
 
 /* Static description of a status code. */

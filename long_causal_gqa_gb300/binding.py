@@ -45,6 +45,8 @@ class h3gqa_plan(ctypes.Structure):
         ("algorithmic_bytes", ctypes.c_double),
         ("tokens_per_unit", ctypes.c_int32),
         ("max_kv_tiles", ctypes.c_int32),
+        ("heads_per_tile", ctypes.c_int32),
+        ("rows_per_tile", ctypes.c_int32),
     ]
 
 
@@ -53,7 +55,7 @@ class h3gqa_options(ctypes.Structure):
         ("causal", ctypes.c_int32),
         ("out_layout", ctypes.c_int32),
         ("out_int8", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("kv_head_begin", ctypes.c_int32),
         ("o_scale", ctypes.c_void_p),
         ("q_norm_weight", ctypes.c_void_p),
         ("k_norm_weight", ctypes.c_void_p),
@@ -61,7 +63,8 @@ class h3gqa_options(ctypes.Structure):
         ("rope_sin", ctypes.c_void_p),
         ("k_out", ctypes.c_void_p),
         ("norm_eps", ctypes.c_float),
-        ("reserved2", ctypes.c_int32),
+        ("kv_head_count", ctypes.c_int32),
+        ("status", ctypes.c_void_p),
     ]
 
 
@@ -142,12 +145,15 @@ def h3gqa_attention_plan(cu_seqlens, n_q_heads, n_kv_heads, head_dim=128, causal
 
 
 def make_options(causal=True, out_layout=H3GQA_LAYOUT_HEAD_MAJOR, out_int8=False,
-                 o_scale_ptr=None, reserved=0, q_norm_ptr=None, k_norm_ptr=None, cos_ptr=None,
-                 sin_ptr=None, k_out_ptr=None, norm_eps=1e-6, reserved2=0):
+                 o_scale_ptr=None, kv_head_begin=0, q_norm_ptr=None, k_norm_ptr=None,
+                 cos_ptr=None, sin_ptr=None, k_out_ptr=None, norm_eps=1e-6, kv_head_count=0,
+                 status_ptr=None):
+    """An h3gqa_options value (pointers as ints or None; see include/h3gqa.h)."""
     return h3gqa_options(1 if causal else 0, int(out_layout), 1 if out_int8 else 0,
-                         int(reserved), o_scale_ptr or None, q_norm_ptr or None,
+                         int(kv_head_begin), o_scale_ptr or None, q_norm_ptr or None,
                          k_norm_ptr or None, cos_ptr or None, sin_ptr or None,
-                         k_out_ptr or None, float(norm_eps), int(reserved2))
+                         k_out_ptr or None, float(norm_eps), int(kv_head_count),
+                         status_ptr or None)
 
 
 def h3gqa_attention_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, cu_seqlens, n_q_heads, n_kv_heads,
@@ -190,11 +196,23 @@ def _cu_total(cu_seqlens):
     return int(vals[-1])
 
 
+def shard_heads(n_kv_heads, world, rank):
+    """KV heads [begin, begin + count) of rank `rank` out of `world` when the
+    heads are split into contiguous, balanced ranges (sizes differ by at most
+    one; a rank gets count 0 when there are more ranks than heads)."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("need 0 <= rank < world")
+    base, extra = divmod(int(n_kv_heads), int(world))
+    begin = rank * base + min(rank, extra)
+    return begin, base + (1 if rank < extra else 0)
+
+
 def check_tensors(q, k, v, cu_seqlens, q_norm_weight=None, k_norm_weight=None, rope_cos=None,
                   rope_sin=None, k_out=None, o=None, lse=None, o_shape=None):
-    """Shape, dtype and layout checks of the torch front ends. The C ABI takes
-    raw pointers and cannot see sizes, so a short table or output here would
-    be read or written out of bounds on the device; these checks run first."""
+    """Shape, dtype, layout and placement checks of the torch front ends. The
+    C ABI takes raw pointers and cannot see sizes or devices, so a short
+    table or output here would be read or written out of bounds on the
+    device; these checks run first."""
     import torch
     if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
         raise ValueError("q, k, v must be [heads, T, head_dim]")
@@ -218,6 +236,17 @@ def check_tensors(q, k, v, cu_seqlens, q_norm_weight=None, k_norm_weight=None, r
     if o is not None and (tuple(o.shape) != tuple(o_shape or q.shape) or
                           o.dtype != torch.bfloat16 or not o.is_contiguous()):
         raise ValueError("o must be a contiguous bf16 tensor shaped like q")
+    for t in (q_norm_weight, k_norm_weight, rope_cos, rope_sin, k_out, o, lse, k, v):
+        if t is not None and t.device != q.device:
+            raise ValueError("every tensor must be on q's device (%s); got %s" % (q.device, t.device))
+    if k_out is not None and k_out.data_ptr() != k.data_ptr() and k_out.numel() > 0:
+        def span(t):
+            return t.data_ptr(), t.data_ptr() + t.numel() * t.element_size()
+        a0, a1 = span(k_out)
+        for name, t in (("q", q), ("k", k), ("v", v)):
+            b0, b1 = span(t)
+            if a0 < b1 and b0 < a1:
+                raise ValueError("k_out must be k itself or a buffer that does not overlap %s" % name)
     return hq, hkv, T, d
 
 
@@ -227,57 +256,78 @@ def _check_cuda(*tensors):
             raise ValueError("all tensors must be CUDA tensors")
 
 
+def _finish(status, stream, where):
+    """Waits for `stream` and raises if this call's status word is non-zero."""
+    stream.synchronize()
+    if int(status.item()) != 0:
+        raise H3GQAError(H3GQA_ERR_TIMEOUT, where)
+
+
 def attention_fwd(q, k, v, cu_seqlens, scale=None, causal=True, token_major=False,
                   out_int8=False, stream=None, q_norm_weight=None, k_norm_weight=None,
-                  rope_cos=None, rope_sin=None, norm_eps=1e-6, k_out=None):
+                  rope_cos=None, rope_sin=None, norm_eps=1e-6, k_out=None, kv_heads=None,
+                  o=None, lse=None, o_scale=None, check=True):
     """Torch front end of h3gqa_attention_fwd. Returns (o, lse, o_scale):
     o bf16 (or int8 codes) in [Hq,T,D] or [T,Hq,D] order, lse fp32 [Hq,T],
     o_scale fp32 [Hq,T] / [T,Hq] for int8 output (else None). With the Q/K
     prologue (norm weights: bf16 [D] CUDA; rope tables: fp32 [T, D/2] CUDA)
     the prepared keys go to k_out (allocated if not given; read it back as
-    the post-prologue key cache)."""
+    the post-prologue key cache).
+
+    kv_heads = (begin, count) computes that head shard only (rows of the other
+    heads in o / lse / o_scale are left as they were; pass the buffers to
+    fill them across calls). With check=True (the default) the call waits for
+    its stream and raises H3GQAError(H3GQA_ERR_TIMEOUT) if the kernel gave up
+    on a bounded wait, using a status word of its own; check=False returns
+    at once (the work stays queued) and reports nothing."""
     import torch
     hq, hkv, T, d = check_tensors(q, k, v, cu_seqlens, q_norm_weight, k_norm_weight, rope_cos,
-                                  rope_sin, k_out)
-    _check_cuda(q, k, v, q_norm_weight, k_norm_weight, rope_cos, rope_sin, k_out)
+                                  rope_sin, k_out, lse=lse)
+    _check_cuda(q, k, v, q_norm_weight, k_norm_weight, rope_cos, rope_sin, k_out, o, lse, o_scale)
     if scale is None:
         scale = d ** -0.5
     shape = (T, hq, d) if token_major else (hq, T, d)
-    o = torch.empty(shape, dtype=torch.int8 if out_int8 else torch.bfloat16, device=q.device)
-    lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
-    o_scale = None
-    if out_int8:
+    odt = torch.int8 if out_int8 else torch.bfloat16
+    if o is None:
+        o = torch.empty(shape, dtype=odt, device=q.device)
+    elif tuple(o.shape) != shape or o.dtype != odt or not o.is_contiguous() or o.device != q.device:
+        raise ValueError("o must be a contiguous %s tensor of shape %s on %s" % (odt, shape, q.device))
+    if lse is None:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    if out_int8 and o_scale is None:
         o_scale = torch.empty(shape[:2], dtype=torch.float32, device=q.device)
+    if o_scale is not None and (not out_int8 or tuple(o_scale.shape) != shape[:2] or
+                                o_scale.dtype != torch.float32 or not o_scale.is_contiguous() or
+                                o_scale.device != q.device):
+        raise ValueError("o_scale must be a contiguous fp32 %s tensor on %s, with out_int8"
+                         % (shape[:2], q.device))
     prep_k = k_norm_weight is not None or rope_cos is not None
     if prep_k and k_out is None:
         k_out = torch.empty_like(k)
+    kv_begin, kv_count = kv_heads if kv_heads is not None else (0, 0)
+    status = torch.zeros(1, dtype=torch.int32, device=q.device) if check else None
     ptr = lambda t: t.data_ptr() if t is not None else None
     opts = make_options(causal, H3GQA_LAYOUT_TOKEN_MAJOR if token_major else
-                        H3GQA_LAYOUT_HEAD_MAJOR, out_int8, ptr(o_scale), 0, ptr(q_norm_weight),
-                        ptr(k_norm_weight), ptr(rope_cos), ptr(rope_sin),
-                        ptr(k_out) if prep_k else None, norm_eps)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device)
-    h3gqa_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                        cu_seqlens, hq, hkv, d, float(scale), opts, stream.cuda_stream)
+                        H3GQA_LAYOUT_HEAD_MAJOR, out_int8, ptr(o_scale), kv_begin,
+                        ptr(q_norm_weight), ptr(k_norm_weight), ptr(rope_cos), ptr(rope_sin),
+                        ptr(k_out) if prep_k else None, norm_eps, kv_count, ptr(status))
+    with torch.cuda.device(q.device):
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        h3gqa_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), cu_seqlens, hq, hkv, d, float(scale), opts,
+                            stream.cuda_stream)
+        if check:
+            _finish(status, stream, "h3gqa_attention_fwd")
     return o, lse, o_scale
 
 
-def causal_gqa_fwd(q, k, v, cu_seqlens, scale=None, o=None, lse=None, stream=None):
+def causal_gqa_fwd(q, k, v, cu_seqlens, scale=None, o=None, lse=None, stream=None, check=True):
     """Torch front end: q [Hq,T,D], k/v [Hkv,T,D] bf16 CUDA tensors (contiguous),
     cu_seqlens host ints. Returns (o [Hq,T,D] bf16, lse [Hq,T] fp32) on q's device,
-    queued on `stream` (default: torch's current stream)."""
-    import torch
-    hq, hkv, T, d = check_tensors(q, k, v, cu_seqlens, o=o, lse=lse)
-    _check_cuda(q, k, v, o, lse)
-    if scale is None:
-        scale = d ** -0.5
-    if o is None:
-        o = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device)
-    h3gqa_causal_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                     cu_seqlens, hq, hkv, d, float(scale), stream.cuda_stream)
+    queued on `stream` (default: torch's current stream). check=True (the
+    default) waits for the stream and raises H3GQAError(H3GQA_ERR_TIMEOUT) if
+    the kernel gave up on a bounded wait; check=False leaves the work queued."""
+    o, lse, _ = attention_fwd(q, k, v, cu_seqlens, scale, o=o, lse=lse, stream=stream,
+                              check=check)
     return o, lse

@@ -11,10 +11,15 @@
 // on-chip state per query row is O(tile) and there is no length bound.
 //
 // Work decomposition ("pack-GQA"): a query tile is 128 MMA rows made of the
-// G = Hq/Hkv query heads of one KV head times 128/G consecutive tokens (row
-// r = head (r / (128/G)), token (r % (128/G))). A unit is two such tiles
-// (256/G consecutive tokens) plus every 128-key tile at or before its last
-// token, so each K/V tile staged in shared memory feeds all G query heads.
+// query heads of one head group times consecutive tokens. A head group is
+// `tile_heads` query heads that read the same KV head: all G = Hq/Hkv of them
+// when G <= 128 (more generally the largest divisor of G that is <= 128, so a
+// KV head with G > 128 heads has G/tile_heads groups). A tile holds
+// tile_tokens = floor(128 / tile_heads) tokens (row r = head r / tile_tokens
+// of the group, token r % tile_tokens); rows past tile_heads * tile_tokens
+// are unused. A unit is two such tiles (2 * tile_tokens consecutive tokens)
+// plus every 128-key tile up to its last token, so each K/V tile staged in
+// shared memory feeds every query head of the group.
 //
 // CTA roles (352 threads, one CTA per SM, persistent over units):
 //   warps 0-3  softmax for query tile 0 (thread = MMA row = TMEM lane)
@@ -30,6 +35,12 @@
 #include "ptx_sm103a.cuh"
 
 namespace h3gqa {
+
+// The unit schedule below also compiles as host code, so that it can be
+// walked on the CPU.
+#define H3GQA_HD __host__ __device__ __forceinline__
+
+H3GQA_HD int imin(int a, int b) { return a < b ? a : b; }
 
 constexpr int kHeadDim = 128;
 constexpr int kRows = 128;                 // MMA M: query rows per tile
@@ -73,12 +84,13 @@ constexpr uint64_t kDrainNs = 2000000000ull;        // wall time allowed for in-
 __device__ unsigned int g_timeout_flags;
 
 struct FwdParams {
-    CUtensorMap map_q;      // q [Hq][T][128], box {64, 128/G, G}
+    CUtensorMap map_q;      // q [Hq][T][128], box {64, tile_tokens, tile_heads}
     CUtensorMap map_k;      // k [Hkv][T][128], box {64, 128, 1}
     CUtensorMap map_v;      // v [Hkv][T][128], box {64, 128, 1}
     void *o;                // bf16 (or int8 codes) [Hq][T][128] or [T][Hq][128]
     float *lse;             // fp32 [Hq][T]
     float *o_scale;         // int8 output only: one fp32 scale per (token, head) row
+    unsigned int *status;   // optional per-call word: timeout bits are ORed into it
     int causal;             // 1: key j visible to query i iff j <= i; 0: all keys of the sequence
     int out_token_major;    // 0: o is [Hq][T][128]; 1: o is [T][Hq][128] (o_scale likewise)
     int out_int8;           // 0: bf16 o; 1: int8 codes, o ~= code * o_scale
@@ -93,17 +105,21 @@ struct FwdParams {
     float norm_eps;
     long long total_tokens;
     long long n_units;
-    int n_kv_heads;
-    int group;              // G = Hq / Hkv
-    int tile_tokens;        // 128 / G tokens per query tile
-    int tile_tokens_log2;
+    int n_groups;           // head groups this call covers (a head shard covers a subset)
+    int group0;             // first head group of this call
+    int groups_per_kv;      // head groups per KV head (G / tile_heads)
+    int tile_heads;         // query heads per tile
+    int tile_tokens;        // floor(128 / tile_heads) tokens per query tile
+    int tile_rows;          // tile_heads * tile_tokens used MMA rows (<= 128)
     int unit_tokens;        // 2 * tile_tokens
-    int unit_tokens_log2;
-    int blocks_per_class;   // 128 / unit_tokens: units of one sequence that visit the same number of K/V tiles
+    int pow2;               // unit_tokens is a power of two dividing 128: shift paths below
+    int unit_tokens_log2;   // pow2 only
+    int blocks_per_class;   // pow2 only: 128 / unit_tokens units of one sequence visit the same K/V tiles
     int blocks_per_class_log2;
     int n_seqs;             // non-empty sequences, sorted by length (descending)
-    int c_max;              // most K/V tiles any unit visits
-    int full_windows;       // (n_units / n_kv_heads) / grid: whole windows of the unit schedule
+    int c_max;              // highest cost class (K/V tiles of the longest sequence's last block)
+    int full_windows;       // (n_units / n_groups) / grid: whole windows of the unit schedule
+    unsigned int q_tx_bytes;   // bytes of one unit's two Q tiles as TMA writes them
     float scale_log2;       // scale * log2(e)
     int seq_start[kMaxSeqs];
     int seq_len[kMaxSeqs];
@@ -113,55 +129,70 @@ struct Unit {
     int seq_start;
     int seq_len;
     int block;      // token block index inside the sequence
-    int kv_head;
+    int group;      // head group, relative to the call's first group
 };
 
 // Walks the global longest-first order of block slots (a slot is one token
-// block of one sequence; it becomes a unit once a KV head is attached).
-// Slots are grouped by cost class c (= K/V tiles visited, from c_max down to
-// 1); inside a class by sequence (longest first), then block. Without the
-// causal rule every slot of a sequence costs the same: longest sequence
-// first, then block. Every role of a CTA runs the same walk, so no schedule
-// is stored anywhere. Successive seeks must not go backwards.
+// block of one sequence; it becomes a unit once a head group is attached).
+// Slots are grouped by cost class c (= K/V tiles up to the block's last
+// token, from c_max down to 1); inside a class by sequence (longest first),
+// then block. Block k of U tokens reaches tile floor((kU + U - 1) / 128), so
+// class c starts at block floor(128 (c - 1) / U); when U divides 128 every
+// class holds 128 / U blocks. Without the causal rule every slot of a
+// sequence costs the same: longest sequence first, then block. Every role of
+// a CTA runs the same walk, so no schedule is stored anywhere. Successive
+// seeks must not go backwards.
 struct UnitWalker {
     int c;
     int i;
     int base;       // first slot of the current (class, sequence) group; slots fit in int
 
-    __device__ __forceinline__ void init(const FwdParams &p)
+    H3GQA_HD void init(const FwdParams &p)
     {
         c = p.c_max;
         i = 0;
         base = 0;
     }
 
-    __device__ __forceinline__ int blocks_of(const FwdParams &p, int seq) const
+    H3GQA_HD int blocks_of(const FwdParams &p, int seq) const
     {
-        return (p.seq_len[seq] + p.unit_tokens - 1) >> p.unit_tokens_log2;
+        const int n = p.seq_len[seq] + p.unit_tokens - 1;
+        return p.pow2 ? n >> p.unit_tokens_log2 : n / p.unit_tokens;
     }
 
-    __device__ __forceinline__ int blocks_in_class(const FwdParams &p, int cls, int seq) const
+    // first block of cost class cls (any sequence long enough to have it)
+    H3GQA_HD int class_lo(const FwdParams &p, int cls) const
     {
-        const int lo = (cls - 1) << p.blocks_per_class_log2;
-        const int hi = min(cls << p.blocks_per_class_log2, blocks_of(p, seq));
+        return p.pow2 ? (cls - 1) << p.blocks_per_class_log2 : (kKeys * (cls - 1)) / p.unit_tokens;
+    }
+
+    H3GQA_HD int blocks_in_class(const FwdParams &p, int cls, int seq) const
+    {
+        const int lo = class_lo(p, cls);
+        const int hi = imin(class_lo(p, cls + 1), blocks_of(p, seq));
         return hi > lo ? hi - lo : 0;
     }
 
-    // slot must not decrease from one call to the next, and slot < n_units / n_kv_heads.
-    __device__ __forceinline__ Unit seek(const FwdParams &p, int slot)
+    // slot must not decrease from one call to the next, and slot < n_units / n_groups.
+    H3GQA_HD Unit seek(const FwdParams &p, int slot)
     {
         Unit r;
         if (p.causal && p.n_seqs == 1) {
-            // One sequence: the top class holds the blocks past the last
-            // whole class, every lower class blocks_per_class of them.
             const int nblk = blocks_of(p, 0);
-            const int top = nblk - ((p.c_max - 1) << p.blocks_per_class_log2);
-            if (slot < top) {
-                r.block = ((p.c_max - 1) << p.blocks_per_class_log2) + slot;
+            if (p.pow2) {
+                // One sequence: the top class holds the blocks past the last
+                // whole class, every lower class blocks_per_class of them.
+                const int top = nblk - ((p.c_max - 1) << p.blocks_per_class_log2);
+                if (slot < top) {
+                    r.block = ((p.c_max - 1) << p.blocks_per_class_log2) + slot;
+                } else {
+                    const int s2 = slot - top;
+                    const int cls = p.c_max - 1 - (s2 >> p.blocks_per_class_log2);
+                    r.block = ((cls - 1) << p.blocks_per_class_log2) + (s2 & (p.blocks_per_class - 1));
+                }
             } else {
-                const int s2 = slot - top;
-                const int cls = p.c_max - 1 - (s2 >> p.blocks_per_class_log2);
-                r.block = ((cls - 1) << p.blocks_per_class_log2) + (s2 & (p.blocks_per_class - 1));
+                // block cost grows with the block index: last block first
+                r.block = nblk - 1 - slot;
             }
         } else if (!p.causal) {
             for (;;) {
@@ -182,72 +213,82 @@ struct UnitWalker {
                     --c;
                 }
             }
-            r.block = ((c - 1) << p.blocks_per_class_log2) + (slot - base);
+            r.block = class_lo(p, c) + (slot - base);
         }
         r.seq_start = p.seq_start[i];
         r.seq_len = p.seq_len[i];
-        r.kv_head = 0;
+        r.group = 0;
         return r;
     }
 };
 
-// Key tiles a unit visits: up to its last token (causal), or the whole
-// sequence.
-__device__ __forceinline__ int unit_kv_tiles(const FwdParams &p, const Unit &un)
+// Key tiles a unit visits: up to its last token inside the sequence
+// (causal), or the whole sequence.
+H3GQA_HD int unit_kv_tiles(const FwdParams &p, const Unit &un)
 {
-    return p.causal ? (un.block * p.unit_tokens) / kKeys + 1 : (un.seq_len + kKeys - 1) / kKeys;
+    const int last = imin(un.block * p.unit_tokens + p.unit_tokens, un.seq_len) - 1;
+    return p.causal ? last / kKeys + 1 : (un.seq_len + kKeys - 1) / kKeys;
 }
 
 // Round r of the static schedule hands CTA x the unit index r*grid + x on
 // even rounds and r*grid + (grid-1-x) on odd ones (a snake), which evens out
 // the falling unit costs of the longest-first order.
-__device__ __forceinline__ long long unit_of_round(long long r)
+H3GQA_HD long long unit_of_round(long long r, int grid, int cta)
 {
-    const long long g = gridDim.x;
-    const long long x = blockIdx.x;
+    const long long g = grid;
+    const long long x = cta;
     return r * g + ((r & 1) ? (g - 1 - x) : x);
 }
 
-// Maps unit indices to (slot, KV head). The slot order is cut into windows of
-// grid slots; inside a window the KV head is the slowest index, so the grid's
-// CTAs, which run one round at a time, work on one KV head and share its K/V
-// tiles in L2 (with the head fastest, a round spans every head and a long
-// sequence's K/V no longer fits in L2). Round r of window r / Hkv runs head
-// r mod Hkv on slot x or grid-1-x; even and odd rounds keep a walker each, so
-// both only move forward. The last, partial window keeps the head fastest.
+// Maps unit indices to (slot, head group). The slot order is cut into windows
+// of grid slots; inside a window the head group is the slowest index, so the
+// grid's CTAs, which run one round at a time, work on one group and share its
+// K/V tiles in L2 (with the group fastest, a round spans every KV head and a
+// long sequence's K/V no longer fits in L2). Round r of window r / n_groups
+// runs group r mod n_groups on slot x or grid-1-x; even and odd rounds keep a
+// walker each, so both only move forward. The last, partial window keeps the
+// group fastest.
 struct Schedule {
     UnitWalker even, odd;
 
-    __device__ __forceinline__ void init(const FwdParams &p)
+    H3GQA_HD void init(const FwdParams &p)
     {
         even.init(p);
         odd.init(p);
     }
 
-    // The unit of round r (r < n_units < 2^31); r must not decrease between calls.
-    __device__ __forceinline__ Unit at(const FwdParams &p, long long r64)
+    // The unit of round r (r < n_units < 2^31) for CTA `cta` of a grid of
+    // `g`; r must not decrease between calls.
+    H3GQA_HD Unit at(const FwdParams &p, long long r64, int g, int cta)
     {
         const int r = (int)r64;
-        const int g = gridDim.x;
-        const int x = (r & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x;
-        const int w = r / p.n_kv_heads;
+        const int x = (r & 1) ? g - 1 - cta : cta;
+        const int w = r / p.n_groups;
         Unit un;
         if (w < p.full_windows) {
             un = ((r & 1) ? odd : even).seek(p, w * g + x);
-            un.kv_head = r - w * p.n_kv_heads;
+            un.group = r - w * p.n_groups;
         } else {
-            const int q = (r - p.full_windows * p.n_kv_heads) * g + x;
-            const int qs = q / p.n_kv_heads;
+            const int q = (r - p.full_windows * p.n_groups) * g + x;
+            const int qs = q / p.n_groups;
             un = even.seek(p, p.full_windows * g + qs);
-            un.kv_head = q - qs * p.n_kv_heads;
+            un.group = q - qs * p.n_groups;
         }
         return un;
     }
 };
 static_assert(sizeof(Schedule) == kSchedSlotBytes, "schedule slot size");
 
+// Raises timeout bit `who` in the device-wide flag and in the call's own
+// status word (if it gave one).
+__device__ __forceinline__ void report_timeout(unsigned int *status, unsigned int who)
+{
+    atomicOr(&g_timeout_flags, who);
+    if (status != nullptr) atomicOr(status, who);
+}
+
 __device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int who)
+                                          unsigned int who, unsigned int *status)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -257,7 +298,7 @@ __device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, volatil
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > kWaitNs) {
             *abort_flag = 1;
-            atomicOr(&g_timeout_flags, who);
+            report_timeout(status, who);
             return false;
         }
     }
@@ -266,12 +307,12 @@ __device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, volatil
 
 // Waits without giving up early on an abort (teardown: copies or MMAs in
 // flight must finish before the CTA releases its memory); bounded in time.
-__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned int *status)
 {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait_capped(bar, parity)) {
         if (global_timer_ns() - t0 > kDrainNs) {
-            atomicOr(&g_timeout_flags, 8u);
+            report_timeout(status, 8u);
             return false;
         }
     }
@@ -281,9 +322,9 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity)
 // All 32 lanes wait; the result is agreed across the warp so that the
 // .sync.aligned TMEM instructions after it never run on a partial warp.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int who)
+                                          unsigned int who, unsigned int *status)
 {
-    bool ok = wait_poll(bar, parity, abort_flag, who);
+    bool ok = wait_poll(bar, parity, abort_flag, who, status);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) *abort_flag = 1;
     return ok;
@@ -304,7 +345,17 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    unsigned int *const status = p.status;
 
+    if (p.tile_rows < kRows) {
+        // Query tiles with unused MMA rows: TMA never writes those rows, so
+        // they are zeroed once here (their scores stay finite; every MMA row
+        // is independent of the others, and unused rows are never stored).
+        uint4 *q4 = reinterpret_cast<uint4 *>(smem + kQOff);
+        for (int i = threadIdx.x; i < (int)(2 * kTileBytes / 16); i += kThreads)
+            q4[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQFull), 1);
         mbar_init(bar(kBarQEmpty), 2);              // one commit per MMA issuer
@@ -349,19 +400,19 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             int last_q_parity = -1;
             bool ok = true;
             for (long long r = 0; ok; ++r) {
-                const long long u = unit_of_round(r);
+                const long long u = unit_of_round(r, gridDim.x, blockIdx.x);
                 if (u >= p.n_units) break;
-                const Unit un = w.at(p, r);
+                const Unit un = w.at(p, r, gridDim.x, blockIdx.x);
                 const int tb = un.block * p.unit_tokens;
                 const int n_kv = unit_kv_tiles(p, un);
-                if (!wait_poll(bar(kBarQEmpty), (unit_it & 1) ^ 1, abort_flag, 1u)) { ok = false; break; }
+                if (!wait_poll(bar(kBarQEmpty), (unit_it & 1) ^ 1, abort_flag, 1u, status)) { ok = false; break; }
                 uint32_t rope_bytes = 0;
                 const long long tok0 = (long long)un.seq_start + tb;
                 if (p.stage_rope) {
                     const long long rows = min((long long)p.unit_tokens, p.total_tokens - tok0);
                     rope_bytes = (uint32_t)rows * kRopeRowBytes;
                 }
-                mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes + 2 * rope_bytes);
+                mbar_arrive_expect_tx(bar(kBarQFull), p.q_tx_bytes + 2 * rope_bytes);
                 last_q_parity = unit_it & 1;
                 // one copy per token row (cos, then sin), into the padded rows
                 for (uint32_t rr = 0; rr < rope_bytes / kRopeRowBytes; ++rr) {
@@ -371,23 +422,25 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     bulk_load(sbase + kRopeOff + kRopeBytes / 2 + rr * kRopeStride, p.rope_sin + tr * (kHeadDim / 2),
                               kRopeRowBytes, bar(kBarQFull));
                 }
+                const int grp = p.group0 + un.group;               // absolute head group
+                const int kvh = p.groups_per_kv == 1 ? grp : grp / p.groups_per_kv;
                 for (int t = 0; t < 2; ++t)
                     for (int h = 0; h < 2; ++h)
                         tma_load_3d(sQ + (uint32_t)(t * 2 + h) * kSubTileBytes, &p.map_q,
                                     bar(kBarQFull), 64 * h, un.seq_start + tb + t * p.tile_tokens,
-                                    un.kv_head * p.group);
+                                    grp * p.tile_heads);
                 for (int j = 0; j < n_kv && ok; ++j) {
                     for (int kind = 0; kind < 2; ++kind) {
                         const uint32_t s = kv_it % kStages;
                         const uint32_t ph = (kv_it / kStages) & 1;
-                        if (!wait_poll(bar(kBarKvEmpty + s), ph ^ 1, abort_flag, 1u)) { ok = false; break; }
+                        if (!wait_poll(bar(kBarKvEmpty + s), ph ^ 1, abort_flag, 1u, status)) { ok = false; break; }
                         mbar_arrive_expect_tx(bar(kBarKvFull + s), kTileBytes);
                         last_kv_parity[s] = (int)ph;
                         const CUtensorMap *map = kind ? &p.map_v : &p.map_k;
                         for (int h = 0; h < 2; ++h)
                             tma_load_3d(sKV + s * kTileBytes + (uint32_t)h * kSubTileBytes, map,
                                         bar(kBarKvFull + s), 64 * h, un.seq_start + j * kKeys,
-                                        un.kv_head);
+                                        kvh);
                         ++kv_it;
                     }
                 }
@@ -396,8 +449,8 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             if (!ok) {
                 // Let every copy already issued land before the CTA exits.
                 for (int s = 0; s < kStages; ++s)
-                    if (last_kv_parity[s] >= 0) wait_drain(bar(kBarKvFull + s), (uint32_t)last_kv_parity[s]);
-                if (last_q_parity >= 0) wait_drain(bar(kBarQFull), (uint32_t)last_q_parity);
+                    if (last_kv_parity[s] >= 0) wait_drain(bar(kBarKvFull + s), (uint32_t)last_kv_parity[s], status);
+                if (last_q_parity >= 0) wait_drain(bar(kBarQFull), (uint32_t)last_q_parity, status);
             }
         }
         __syncwarp();
@@ -439,7 +492,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                         if (*abort_flag) return false;
                         if (global_timer_ns() - t0 > kWaitNs) {
                             *abort_flag = 1;
-                            atomicOr(&g_timeout_flags, 2u);
+                            report_timeout(status, 2u);
                             return false;
                         }
                     }
@@ -481,17 +534,17 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             const unsigned who = 2u;
 
             for (long long r = 0; ok; ++r) {
-                const long long u = unit_of_round(r);
+                const long long u = unit_of_round(r, gridDim.x, blockIdx.x);
                 if (u >= p.n_units) break;
-                const Unit un = w.at(p, r);
+                const Unit un = w.at(p, r, gridDim.x, blockIdx.x);
                 const int n_kv = unit_kv_tiles(p, un);
-                if (!wait_poll(bar(p.prep_q ? kBarQReady + t : kBarQFull), unit_it & 1, abort_flag, who)) {
+                if (!wait_poll(bar(p.prep_q ? kBarQReady + t : kBarQFull), unit_it & 1, abort_flag, who, status)) {
                     ok = false;
                     break;
                 }
                 {
                     const uint32_t s = kv_it % kStages;
-                    if (!wait_poll(bar(kBarKvFull + s), (kv_it / kStages) & 1, abort_flag, who)) { ok = false; break; }
+                    if (!wait_poll(bar(kBarKvFull + s), (kv_it / kStages) & 1, abort_flag, who, status)) { ok = false; break; }
                     if (!take_turn()) { ok = false; break; }
                     tc_fence_after_sync();
                     issue_s(s);
@@ -505,9 +558,9 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     const bool more = j + 1 < n_kv;
                     const uint32_t itk = itv + 1u;
                     const uint32_t sk = itk % kStages;
-                    if (!wait_poll(bar(kBarKvFull + sv), (itv / kStages) & 1, abort_flag, who)) { ok = false; break; }
-                    if (more && !wait_poll(bar(kBarKvFull + sk), (itk / kStages) & 1, abort_flag, who)) { ok = false; break; }
-                    if (!wait_poll(bar(kBarPFull + t), p_phase & 1, abort_flag, who)) { ok = false; break; }
+                    if (!wait_poll(bar(kBarKvFull + sv), (itv / kStages) & 1, abort_flag, who, status)) { ok = false; break; }
+                    if (more && !wait_poll(bar(kBarKvFull + sk), (itk / kStages) & 1, abort_flag, who, status)) { ok = false; break; }
+                    if (!wait_poll(bar(kBarPFull + t), p_phase & 1, abort_flag, who, status)) { ok = false; break; }
                     ++p_phase;
                     if (!take_turn()) { ok = false; break; }
                     tc_fence_after_sync();
@@ -525,7 +578,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             }
             // Nothing this lane issued may still be running when TMEM is freed.
             mma_commit(bar(kBarDrain + t));
-            wait_drain(bar(kBarDrain + t), 0);
+            wait_drain(bar(kBarDrain + t), 0, status);
         }
         __syncwarp();
     } else {
@@ -535,18 +588,19 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
         const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_bits + (uint32_t)t * 128u;
         const uint32_t tO = tmem + lane_bits + 256u + (uint32_t)t * 128u;
-        const int head_in_group = row >> p.tile_tokens_log2;
-        const int tok_in_tile = row & (p.tile_tokens - 1);
+        const int head_in_group = row / p.tile_tokens;
+        const int tok_in_tile = row - head_in_group * p.tile_tokens;
+        const bool row_used = row < p.tile_rows;
         const float c = p.scale_log2;
         // Q prologue for this thread's row of query tile t of unit `uq`: wait
         // for the tile, RMS-normalise the row and/or rotate it in place in
         // shared memory, then hand the tile to the MMA issuer (the writes go
         // through the generic proxy, the MMA reads through the async proxy).
         auto prep_q = [&](const Unit &uq, uint32_t q_it) -> bool {
-            if (!wait_warp(bar(kBarQFull), q_it & 1, abort_flag, 4u)) return false;
+            if (!wait_warp(bar(kBarQFull), q_it & 1, abort_flag, 4u, status)) return false;
             const long long tokg = (long long)uq.seq_start + uq.block * p.unit_tokens +
                                    t * p.tile_tokens + tok_in_tile;
-            if (tokg < p.total_tokens) {
+            if (row_used && tokg < p.total_tokens) {
                 uint8_t *rowp = smem + kQOff + (uint32_t)t * kTileBytes + (uint32_t)row * 128u;
                 // 16-byte chunk cc (8 values) of half h of this row, in the
                 // 128-byte swizzled layout TMA wrote
@@ -636,19 +690,24 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
         // Each unit is looked up at the end of the one before, where the
         // score rows are no longer live.
         Unit un;
-        if (unit_of_round(0) < p.n_units) {
-            un = w.at(p, 0);
+        const int grid = gridDim.x, cta = blockIdx.x;
+        if (unit_of_round(0, grid, cta) < p.n_units) {
+            un = w.at(p, 0, grid, cta);
             if (p.prep_q) ok = prep_q(un, 0);
         }
         for (long long r = 0; ok; ++r) {
-            if (unit_of_round(r) >= p.n_units) break;
+            if (unit_of_round(r, grid, cta) >= p.n_units) break;
             const int tb = un.block * p.unit_tokens;
             const int n_kv = unit_kv_tiles(p, un);
             const int tok = tb + t * p.tile_tokens + tok_in_tile;   // token inside its sequence
+            // key tiles from here on may hold keys a row must not see: past
+            // the unit's first token (causal; one tile when the unit size
+            // divides 128, at most two otherwise) or past the sequence end
+            const int mask_from = p.causal ? (tb >> 7) : n_kv - 1;
             float m = -INFINITY;   // running max of the scaled logits, log2 units
             float l = 0.f;         // running sum of exp2(logit - m)
             for (int j = 0; j < n_kv; ++j) {
-                if (!wait_warp(bar(kBarSFull + t), s_phase & 1, abort_flag, 4u)) { ok = false; break; }
+                if (!wait_warp(bar(kBarSFull + t), s_phase & 1, abort_flag, 4u, status)) { ok = false; break; }
                 ++s_phase;
                 tc_fence_after_sync();
                 float s[kKeys];
@@ -658,9 +717,9 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
 #pragma unroll
                     for (int i = 0; i < kKeys; ++i) s[i] = __uint_as_float(sr[i]);
                 }
-                if (j == n_kv - 1) {
-                    // last tile: key (j*128 + i) is visible iff it is <= tok
-                    // (causal) or inside the sequence (bidirectional)
+                if (j >= mask_from) {
+                    // key (j*128 + i) is visible iff it is <= tok (causal) or
+                    // inside the sequence (bidirectional)
                     const int lim = (p.causal ? tok : un.seq_len - 1) - j * kKeys;
 #pragma unroll
                     for (int i = 0; i < kKeys; ++i)
@@ -723,11 +782,11 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             // The next unit's Q tile lands while this unit's last P.V and the
             // epilogue run; its rotary table rows are pulled into L1 now.
             ++q_it;
-            const bool has_next = unit_of_round(r + 1) < p.n_units;
+            const bool has_next = unit_of_round(r + 1, grid, cta) < p.n_units;
             const bool prep_next = p.prep_q && has_next;
             Unit next_un = un;
             if (prep_next) {
-                next_un = w.at(p, r + 1);
+                next_un = w.at(p, r + 1, grid, cta);
                 if (p.rope_cos != nullptr && !p.stage_rope) {
                     const long long tn = (long long)next_un.seq_start + next_un.block * p.unit_tokens +
                                          t * p.tile_tokens + tok_in_tile;
@@ -741,12 +800,12 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 }
             }
             // ------------------------------------------------------ epilogue
-            if (!wait_warp(bar(kBarOFull + t), o_phase & 1, abort_flag, 4u)) { ok = false; break; }
+            if (!wait_warp(bar(kBarOFull + t), o_phase & 1, abort_flag, 4u, status)) { ok = false; break; }
             ++o_phase;
             tc_fence_after_sync();
             const float inv_l = 1.0f / l;
-            const bool valid = tok < un.seq_len;
-            const int head = un.kv_head * p.group + head_in_group;
+            const bool valid = row_used && tok < un.seq_len;
+            const int head = (p.group0 + un.group) * p.tile_heads + head_in_group;
             const long long tok_g = (long long)un.seq_start + tok;
             const long long grow = (long long)head * p.total_tokens + tok_g;          // [Hq][T] index
             const long long orow = p.out_token_major ? tok_g * p.n_q_heads + head : grow;
@@ -806,7 +865,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             if (valid) p.lse[grow] = (m + __log2f(l)) * 0.69314718055994531f;
             tc_fence_before_sync();
             if (prep_next && !prep_q(next_un, q_it)) { ok = false; break; }
-            if (has_next && !prep_next) next_un = w.at(p, r + 1);
+            if (has_next && !prep_next) next_un = w.at(p, r + 1, grid, cta);
             un = next_un;
         }
     }

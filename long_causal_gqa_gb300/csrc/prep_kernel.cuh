@@ -20,9 +20,12 @@ namespace h3gqa {
 constexpr int kPrepThreads = 256;
 
 // One warp per row; lane l holds dims 4l..4l+3, so the rotation partner of
-// lane l < 16 is lane l + 16 (dims i and i + 64).
+// lane l < 16 is lane l + 16 (dims i and i + 64). y may be x itself (keys
+// prepared in place): every lane's loads of a row feed the warp shuffles
+// that come before any store of that row, so no lane overwrites a value
+// another lane has yet to read.
 __global__ void __launch_bounds__(kPrepThreads)
-qk_prep_kernel(const uint16_t *__restrict__ x, uint16_t *y, long long n_rows, long long T,
+qk_prep_kernel(const uint16_t *x, uint16_t *y, long long n_rows, long long T,
                const uint16_t *__restrict__ w, float eps, const float *__restrict__ cosv,
                const float *__restrict__ sinv)
 {

@@ -50,7 +50,7 @@ def test_header_compiles_as_plain_c(tmp_path):
 
 
 def test_version_and_status_strings(lib):
-    assert binding.h3gqa_version() == 10000
+    assert binding.h3gqa_version() == 10100
     for st in range(6):
         assert binding.h3gqa_status_string(st)
     assert binding.h3gqa_status_string(99) == "unknown status"
@@ -64,6 +64,7 @@ def test_plan_headline_shape(lib):
     # block k visits floor(k/4)+1 key tiles: 8 heads * 4 * (1+...+80)
     assert p.n_kv_tiles == 8 * 4 * (80 * 81 // 2)
     assert p.max_kv_tiles == 80
+    assert p.heads_per_tile == 8 and p.rows_per_tile == 128
     assert p.metric_flops == 2.0 * 10231 ** 2 * 64 * 128
     assert p.causal_flops == 2.0 * 64 * 128 * 10231 * 10232
     assert p.exp2_count == 64 * 10231 * 10232 / 2
@@ -86,6 +87,46 @@ def test_plan_varlen_and_groups(lib):
     assert p0.n_units == 0 and p0.total_tokens == 0
 
 
+def _units_and_tiles(lens, hq, hkv):
+    """Units and key tiles counted from the tiling rule by brute force: a
+    tile holds h heads (the largest divisor of G = hq/hkv up to 128) times
+    floor(128/h) tokens, a unit two tiles, and a causal unit visits every key
+    tile up to its last token inside the sequence."""
+    g = hq // hkv
+    h = max(d for d in range(1, min(g, 128) + 1) if g % d == 0)
+    u = 2 * (128 // h)
+    groups = hkv * (g // h)
+    units = tiles = 0
+    for s in lens:
+        for t0 in range(0, s, u):
+            last = min(t0 + u, s) - 1
+            units += groups
+            tiles += groups * (last // 128 + 1)
+    return h, u, units, tiles
+
+
+@pytest.mark.parametrize("lens,hq,hkv", [
+    ((300,), 8, 8),           # G = 1 (MHA): 128 tokens x 1 head, 256-token units
+    ((1000, 77), 64, 64),     # G = 1
+    ((500,), 24, 8),          # G = 3: 42 tokens x 3 heads, 126 rows
+    ((333, 0, 129), 40, 8),   # G = 5: 25 x 5 = 125 rows
+    ((700,), 48, 8),          # G = 6: 21 x 6 = 126 rows
+    ((90,), 96, 1),           # G = 96: 1 token x 96 heads
+    ((90,), 256, 1),          # G = 256: two groups of 128 heads per KV head
+    ((90,), 262, 2),          # G = 131 (prime): one head per tile
+])
+def test_plan_any_group_size(lib, lens, hq, hkv):
+    cu = [0]
+    for s in lens:
+        cu.append(cu[-1] + s)
+    p = binding.h3gqa_make_plan(cu, hq, hkv)
+    h, u, units, tiles = _units_and_tiles(lens, hq, hkv)
+    assert p.heads_per_tile == h and p.rows_per_tile == h * (128 // h)
+    assert p.tokens_per_unit == u
+    assert p.n_units == units and p.n_kv_tiles == tiles
+    assert p.causal_flops == sum(2.0 * hq * 128 * s * (s + 1) for s in lens)
+
+
 @pytest.mark.parametrize("cu,hq,hkv,d,status", [
     ([1, 5], 64, 8, 128, H3GQA_ERR_INVALID_ARG),       # cu[0] != 0
     ([0, 5, 3], 64, 8, 128, H3GQA_ERR_INVALID_ARG),    # decreasing
@@ -93,9 +134,7 @@ def test_plan_varlen_and_groups(lib):
     ([0, 5], 0, 8, 128, H3GQA_ERR_INVALID_ARG),
     ([0, 5], 64, 8, 0, H3GQA_ERR_INVALID_ARG),
     ([0, 5], 64, 8, 64, H3GQA_ERR_UNSUPPORTED),        # head_dim
-    ([0, 5], 8, 8, 128, H3GQA_ERR_UNSUPPORTED),        # G = 1
-    ([0, 5], 24, 8, 128, H3GQA_ERR_UNSUPPORTED),       # G = 3
-    ([0, 5], 256, 1, 128, H3GQA_ERR_UNSUPPORTED),      # G = 256
+    ([0, 5], 64, -8, 128, H3GQA_ERR_INVALID_ARG),
 ])
 def test_plan_rejects(lib, cu, hq, hkv, d, status):
     with pytest.raises(H3GQAError) as e:
@@ -167,7 +206,12 @@ def test_attention_options_rejected_before_cuda(lib):
     bad_opts = [binding.make_options(out_int8=True),                       # no o_scale
                 binding.make_options(out_int8=True, o_scale_ptr=good + 2),  # misaligned o_scale
                 binding.make_options(out_layout=2),
-                binding.make_options(reserved=1)]
+                binding.make_options(kv_head_begin=8),                     # shard past the heads
+                binding.make_options(kv_head_begin=-1),
+                binding.make_options(kv_head_count=-1),
+                binding.make_options(kv_head_count=9),
+                binding.make_options(kv_head_begin=4, kv_head_count=5),
+                binding.make_options(status_ptr=good + 2)]                 # misaligned status
     o = binding.make_options()
     o.causal = 2
     bad_opts.append(o)
@@ -193,8 +237,7 @@ def test_prologue_options_rejected_before_cuda(lib):
            binding.make_options(q_norm_ptr=good + 2),                          # misaligned weight
            binding.make_options(cos_ptr=good + 4, sin_ptr=good, k_out_ptr=good),
            binding.make_options(q_norm_ptr=good, norm_eps=-1.0),
-           binding.make_options(q_norm_ptr=good, norm_eps=float("nan")),
-           binding.make_options(reserved2=3)]
+           binding.make_options(q_norm_ptr=good, norm_eps=float("nan"))]
     for opts in bad:
         assert binding.h3gqa_attention_fwd(options=opts, check=False, **base) == \
             H3GQA_ERR_INVALID_ARG
@@ -202,6 +245,32 @@ def test_prologue_options_rejected_before_cuda(lib):
                               k_out_ptr=good)
     assert binding.h3gqa_attention_fwd(options=ok, check=False,
                                        **dict(base, cu_seqlens=[0])) == H3GQA_OK
+
+
+def test_k_out_overlap_rejected_before_cuda(lib):
+    """k_out may be k itself, but not overlap q, v or part of k (the sizes
+    follow from T, the heads and head_dim: q 64*64*128*2 bytes here)."""
+    q, k, v = 1 << 24, 1 << 26, 1 << 27
+    base = dict(q_ptr=q, k_ptr=k, v_ptr=v, o_ptr=1 << 28, lse_ptr=1 << 29,
+                cu_seqlens=[0, 64], n_q_heads=64, n_kv_heads=8, head_dim=128, scale=0.088)
+    qbytes, kbytes = 64 * 64 * 128 * 2, 8 * 64 * 128 * 2
+    for k_out in (q, q + qbytes - 16, v + 16, k + 16, k - kbytes + 16):
+        opts = binding.make_options(k_norm_ptr=1 << 20, k_out_ptr=k_out)
+        assert binding.h3gqa_attention_fwd(options=opts, check=False, **base) == \
+            H3GQA_ERR_INVALID_ARG, hex(k_out)
+
+
+def test_shard_heads_partition():
+    """Contiguous head ranges: every head exactly once, sizes within one."""
+    for n in (1, 3, 8, 64):
+        for world in (1, 2, 3, 4, 8, 9):
+            parts = [binding.shard_heads(n, world, r) for r in range(world)]
+            heads = [h for b, c in parts for h in range(b, b + c)]
+            assert heads == list(range(n))
+            sizes = [c for _, c in parts]
+            assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        binding.shard_heads(8, 2, 2)
 
 
 def test_cu_seqlens_outside_int32_rejected_in_the_binding(lib):
@@ -227,11 +296,15 @@ def test_front_end_shape_checks_on_cpu_tensors():
         dict(k_out=torch.zeros(2, T, d // 2, dtype=torch.bfloat16)),
         dict(o=torch.zeros(8, T, d + 1, dtype=torch.bfloat16)),
         dict(lse=torch.zeros(8, T + 1)),
+        dict(k_out=q[:2]),                                                   # overlaps q
+        dict(k_out=v),                                                       # is v
+        dict(lse=torch.zeros(8, T, device="meta")),                          # other device
     ]
     for b in bad:
         args = dict(q=q, k=k, v=v, cu_seqlens=[0, T])
         args.update(b)
         with pytest.raises(ValueError):
             binding.check_tensors(**args)
+    assert binding.check_tensors(q, k, v, [0, T], k_out=k) == (8, 2, T, d)   # in place is fine
     with pytest.raises(ValueError):
         binding.attention_fwd(q, k, v, [0, T])          # CPU tensors never reach the library

@@ -54,7 +54,7 @@ def test_threads_on_separate_streams(dev):
                     o, lse, _ = binding.attention_fwd(q, k, v, x["cu_seqlens"], SCALE,
                                                       causal=j["causal"],
                                                       token_major=j["token_major"],
-                                                      stream=stream)
+                                                      stream=stream, check=False)
                     outs.append((o, lse))
             binding.h3gqa_sync_and_check(stream.cuda_stream)
             results[i] = outs

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from long_causal_gqa_gb300 import binding, build
-from long_causal_gqa_gb300.binding import H3GQA_ERR_TIMEOUT, H3GQA_OK
+from long_causal_gqa_gb300.binding import H3GQA_ERR_TIMEOUT, H3GQA_OK, H3GQAError
 from long_causal_gqa_gb300.inputs import make_inputs
 from oracle import causal_gqa as orc
 
@@ -61,3 +61,30 @@ def test_timeout_is_reported_and_context_survives(tiny_wait_lib):
     o64 = o.float().cpu().numpy().astype(np.float64)
     assert (np.abs(o64 - ref_o) <= 1e-2 + 1e-2 * np.abs(ref_o)).all()
     assert np.abs(lse.cpu().numpy() - ref_lse).max() <= 1e-3
+
+
+def test_front_end_raises_on_timeout(tiny_wait_lib, monkeypatch):
+    """The torch front end checks its own call by default: a call whose kernel
+    gives up raises H3GQAError(H3GQA_ERR_TIMEOUT) through its per-call status
+    word; with check=False the call returns and the device-wide flag still
+    records the timeout."""
+    dev = torch.device("cuda:0")
+    x = make_inputs((8000, 333), 64, 8, 128, seed=23)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    monkeypatch.setattr(binding, "_LIB", tiny_wait_lib)
+    with pytest.raises(H3GQAError) as e:
+        binding.causal_gqa_fwd(q, k, v, x["cu_seqlens"], 128 ** -0.5)
+    assert e.value.status == H3GQA_ERR_TIMEOUT
+    with pytest.raises(H3GQAError) as e:
+        binding.attention_fwd(q, k, v, x["cu_seqlens"], 128 ** -0.5, causal=False,
+                              kv_heads=(1, 2))
+    assert e.value.status == H3GQA_ERR_TIMEOUT
+    stream = torch.cuda.current_stream(dev)
+    assert tiny_wait_lib.h3gqa_sync_and_check(stream.cuda_stream) == H3GQA_ERR_TIMEOUT
+    binding.causal_gqa_fwd(q, k, v, x["cu_seqlens"], 128 ** -0.5, check=False)
+    assert tiny_wait_lib.h3gqa_sync_and_check(stream.cuda_stream) == H3GQA_ERR_TIMEOUT
+    assert tiny_wait_lib.h3gqa_sync_and_check(stream.cuda_stream) == H3GQA_OK
+    monkeypatch.undo()
+    # the regular library, checked by default, reports nothing on the same inputs
+    o, lse = binding.causal_gqa_fwd(q, k, v, x["cu_seqlens"], 128 ** -0.5)
+    assert bool(torch.isfinite(lse).all())

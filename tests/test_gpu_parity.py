@@ -2,10 +2,14 @@
 
 Bar (the acceptance rule of the causal GQA target): every output element
 |o - ref| <= 1e-2 + 1e-2*|ref|, every LSE |lse - ref| <= 1e-3 (natural log).
-Small shapes are checked in full; the full-size workloads on sampled rows
-that the oracle computes one by one (first/last rows of every sequence, rows
-on both sides of every 128-token boundary, and seeded random rows), all
-heads. Output buffers carry guard regions that must come back untouched.
+Small shapes are checked in full, and so are the single-sequence full-size
+workloads (S = 7700 and S = 10231: every head, every row). The packed
+varlen workload and S = 32768 are checked on at least three rows of every
+work unit the kernel schedules (a unit is one block of tokens of one
+sequence and one head group): for every block and every query head, the
+block's first and last token and one seeded random token, so a unit that
+is skipped, repeated, or run with the wrong KV head, tokens or sequence
+fails. Output buffers carry guard regions that must come back untouched.
 """
 import numpy as np
 import pytest
@@ -106,6 +110,31 @@ def test_group_sizes(dev, hq, hkv):
     full_check((200, 37), hq, hkv, 900 + hq + hkv, dev)
 
 
+# Group sizes whose tiles do not fill 128 rows or whose units straddle two
+# key tiles: G = 1 (plain multi-head attention: 128 tokens x 1 head, 256-token
+# units), G = 3, 5, 6, 7 (42 x 3, 25 x 5, 21 x 6, 18 x 7 rows), G = 96 (96 of
+# 128 rows), G = 256 (two head groups per KV head) and G = 131 (a prime above
+# 128: one head per tile). Lengths cross several key tiles and end ragged.
+ANY_G = [(8, 8), (64, 64), (24, 8), (40, 8), (48, 8), (56, 8), (96, 1), (256, 1), (262, 2)]
+
+
+@pytest.mark.parametrize("hq,hkv", ANY_G)
+def test_any_group_size_causal(dev, hq, hkv):
+    full_check((700, 0, 37, 1, 300), hq, hkv, 1900 + hq + hkv, dev)
+
+
+@pytest.mark.parametrize("hq,hkv", ANY_G)
+def test_any_group_size_bidirectional(dev, hq, hkv):
+    x = make_inputs((700, 0, 37, 1, 300), hq, hkv, 128, 2900 + hq + hkv)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o, lse, _ = binding.attention_fwd(q, k, v, x["cu_seqlens"], 128 ** -0.5, causal=False)
+    ref_o, ref_lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv,
+                                    128 ** -0.5, causal=False)
+    assert_close(o.float().cpu().numpy().astype(np.float64),
+                 lse.cpu().numpy().astype(np.float64), ref_o, ref_lse,
+                 "bidirectional hq=%d hkv=%d" % (hq, hkv))
+
+
 def test_workload_s512_full(dev):
     w = WORKLOADS["s512"]
     full_check(w.seqlens, w.n_q_heads, w.n_kv_heads, w.seed, dev)
@@ -153,8 +182,11 @@ def test_deterministic_and_stream(dev):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-# ------------------------------------------------------ full size, sampled
+# --------------------------------------------------------------- full size
 def sample_rows(cu, hq, n_random, seed):
+    """Sequence edges, both sides of every 128-token boundary (head rotated
+    along the tokens), seeded random rows and every head at the last token of
+    the longest sequence."""
     rows = set()
     T = int(cu[-1])
     for b in range(len(cu) - 1):
@@ -177,18 +209,61 @@ def sample_rows(cu, hq, n_random, seed):
     return np.array(sorted(rows), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["s7700", "s10231", "varlen4", "s32768_outlier"])
-def test_full_size_workloads_sampled(dev, name):
+def unit_rows(cu, hq, hkv, seed):
+    """At least three rows of every work unit, for every query head: a unit
+    is one block of tokens_per_unit tokens of one sequence for the heads of
+    one group; each (block, query head) pair contributes the block's first
+    and last token (inside the sequence) and one seeded random token of it."""
+    plan = binding.h3gqa_make_plan([int(c) for c in cu], hq, hkv)
+    u = int(plan.tokens_per_unit)
+    rng = np.random.default_rng(seed)
+    out = []
+    heads = np.arange(hq, dtype=np.int64)
+    for b in range(len(cu) - 1):
+        s, e = int(cu[b]), int(cu[b + 1])
+        for t0 in range(s, e, u):
+            t1 = min(t0 + u, e) - 1
+            rand = rng.integers(t0, t1 + 1, hq)
+            for toks in (np.full(hq, t0), np.full(hq, t1), rand):
+                out.append(np.stack([heads, toks.astype(np.int64)], axis=1))
+    rows = np.unique(np.concatenate(out), axis=0)
+    return rows
+
+
+@pytest.mark.parametrize("name", ["s7700", "s10231"])
+def test_full_size_every_row(dev, name):
+    """Every head and every row of the single-sequence full-size workloads
+    against the full fp64 oracle (the call is the one the benchmark times)."""
     w = WORKLOADS[name]
     x = make_workload_inputs(w)
     o_t, lse_t = run_gpu(x, w.n_q_heads, w.n_kv_heads, w.scale, dev, as_numpy=False)
+    assert all_finite(o_t, lse_t)
+    ref_o, ref_lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], w.n_q_heads,
+                                    w.n_kv_heads, w.scale)
+    for h0 in range(0, w.n_q_heads, 8):          # 8 heads at a time bounds the fp64 copies
+        sl = slice(h0, h0 + 8)
+        assert_close(o_t[sl].float().numpy().astype(np.float64),
+                     lse_t[sl].numpy().astype(np.float64), ref_o[sl], ref_lse[sl],
+                     "%s heads %d..%d" % (name, h0, h0 + 7))
+
+
+@pytest.mark.parametrize("name", ["varlen4", "s32768_outlier"])
+def test_full_size_every_unit(dev, name):
+    w = WORKLOADS[name]
+    x = make_workload_inputs(w)
+    o_t, lse_t = run_gpu(x, w.n_q_heads, w.n_kv_heads, w.scale, dev, as_numpy=False)
+    assert all_finite(o_t, lse_t)
     cu = x["cu_seqlens"].numpy()
-    rows = sample_rows(cu, w.n_q_heads, 512, w.seed)
+    rows = unit_rows(cu, w.n_q_heads, w.n_kv_heads, w.seed)
+    plan = binding.h3gqa_make_plan([int(c) for c in cu], w.n_q_heads, w.n_kv_heads)
+    # every (unit, query head) of the schedule has its three rows
+    per_unit = plan.n_units * (w.n_q_heads // w.n_kv_heads)
+    assert len(rows) >= per_unit * 2
+    rows = np.unique(np.concatenate([rows, sample_rows(cu, w.n_q_heads, 0, w.seed)]), axis=0)
     ref_o, ref_lse = orc.causal_gqa_rows(x["q"], x["k"], x["v"], cu, w.n_q_heads,
                                          w.n_kv_heads, w.scale, rows)
     got_o, got_l = rows_of(o_t, lse_t, rows)
     assert_close(got_o, got_l, ref_o, ref_lse, name)
-    assert all_finite(o_t, lse_t)
     # every output row is a convex combination of value rows
     vmax = float(x["v"].float().abs().max())
     assert float(o_t.float().abs().max()) <= vmax * (1 + 1e-2)

@@ -39,9 +39,26 @@ def _cases():
     return out
 
 
+def _cases_any_group():
+    """Group sizes that do not divide 128 (G = 1, 3, 5, 6, 7, 12, 24), whose
+    tiles leave MMA rows unused and whose units may straddle two key tiles."""
+    rng = np.random.default_rng(20261203)
+    out = []
+    for i in range(10):
+        hkv = int(rng.choice([1, 2, 3]))
+        g = int(rng.choice([1, 3, 5, 6, 7, 12, 24]))
+        lens = [int(v) for v in rng.integers(0, 700, int(rng.integers(1, 4)))]
+        if sum(lens) == 0:
+            lens[0] = 301
+        out.append(dict(seqlens=tuple(lens), hq=g * hkv, hkv=hkv, causal=bool(rng.random() < 0.6),
+                        token_major=bool(rng.random() < 0.4), int8=bool(rng.random() < 0.3),
+                        prologue=str(rng.choice(["none", "qn", "rope", "all"])), seed=3200 + i))
+    return out
+
+
 # the rotary path that reads its tables from global memory (G < 8), which the
 # seeded draw above happens not to reach
-CASES = _cases() + [
+CASES = _cases() + _cases_any_group() + [
     dict(seqlens=(333, 0, 200), hq=8, hkv=2, causal=True, token_major=False, int8=False,
          prologue="all", seed=3100),
     dict(seqlens=(1, 451), hq=4, hkv=2, causal=False, token_major=True, int8=True,
