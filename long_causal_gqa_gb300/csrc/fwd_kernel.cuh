@@ -77,6 +77,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if the 
 #define H3GQA_WAIT_NS 2000000000ull
 #endif
 constexpr uint64_t kWaitNs = H3GQA_WAIT_NS;         // wall time before a pipeline wait gives up
+
 constexpr uint64_t kDrainNs = 2000000000ull;        // wall time allowed for in-flight copies to land
 
 // Device-side timeout record (per device, static): bit 0 producer, bit 1
@@ -94,6 +95,7 @@ struct FwdParams {
     int causal;             // 1: key j visible to query i iff j <= i; 0: all keys of the sequence
     int out_token_major;    // 0: o is [Hq][T][128]; 1: o is [T][Hq][128] (o_scale likewise)
     int out_int8;           // 0: bf16 o; 1: int8 codes, o ~= code * o_scale
+    int o_align32;          // o's base is 32-byte aligned (every row then is too)
     int n_q_heads;
     // Q prologue (RMS-norm and/or rotary embedding applied to each Q tile in
     // shared memory right after it lands): prep_q != 0 enables it.
@@ -405,6 +407,27 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 const Unit un = w.at(p, r, gridDim.x, blockIdx.x);
                 const int tb = un.block * p.unit_tokens;
                 const int n_kv = unit_kv_tiles(p, un);
+                const int grp = p.group0 + un.group;               // absolute head group
+                const int kvh = p.groups_per_kv == 1 ? grp : grp / p.groups_per_kv;
+                // K and V of key tile j into the next two ring stages
+                auto load_kv = [&](int j) -> bool {
+                    for (int kind = 0; kind < 2; ++kind) {
+                        const uint32_t s = kv_it % kStages;
+                        const uint32_t ph = (kv_it / kStages) & 1;
+                        if (!wait_poll(bar(kBarKvEmpty + s), ph ^ 1, abort_flag, 1u, status)) return false;
+                        mbar_arrive_expect_tx(bar(kBarKvFull + s), kTileBytes);
+                        last_kv_parity[s] = (int)ph;
+                        const CUtensorMap *map = kind ? &p.map_v : &p.map_k;
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_3d(sKV + s * kTileBytes + (uint32_t)h * kSubTileBytes, map,
+                                        bar(kBarKvFull + s), 64 * h, un.seq_start + j * kKeys, kvh);
+                        ++kv_it;
+                    }
+                    return true;
+                };
+                // The unit's first K/V tile is issued before waiting for the Q
+                // buffer, so it is in flight while the last unit finishes.
+                if (!load_kv(0)) { ok = false; break; }
                 if (!wait_poll(bar(kBarQEmpty), (unit_it & 1) ^ 1, abort_flag, 1u, status)) { ok = false; break; }
                 uint32_t rope_bytes = 0;
                 const long long tok0 = (long long)un.seq_start + tb;
@@ -422,28 +445,14 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     bulk_load(sbase + kRopeOff + kRopeBytes / 2 + rr * kRopeStride, p.rope_sin + tr * (kHeadDim / 2),
                               kRopeRowBytes, bar(kBarQFull));
                 }
-                const int grp = p.group0 + un.group;               // absolute head group
-                const int kvh = p.groups_per_kv == 1 ? grp : grp / p.groups_per_kv;
                 for (int t = 0; t < 2; ++t)
                     for (int h = 0; h < 2; ++h)
                         tma_load_3d(sQ + (uint32_t)(t * 2 + h) * kSubTileBytes, &p.map_q,
                                     bar(kBarQFull), 64 * h, un.seq_start + tb + t * p.tile_tokens,
                                     grp * p.tile_heads);
-                for (int j = 0; j < n_kv && ok; ++j) {
-                    for (int kind = 0; kind < 2; ++kind) {
-                        const uint32_t s = kv_it % kStages;
-                        const uint32_t ph = (kv_it / kStages) & 1;
-                        if (!wait_poll(bar(kBarKvEmpty + s), ph ^ 1, abort_flag, 1u, status)) { ok = false; break; }
-                        mbar_arrive_expect_tx(bar(kBarKvFull + s), kTileBytes);
-                        last_kv_parity[s] = (int)ph;
-                        const CUtensorMap *map = kind ? &p.map_v : &p.map_k;
-                        for (int h = 0; h < 2; ++h)
-                            tma_load_3d(sKV + s * kTileBytes + (uint32_t)h * kSubTileBytes, map,
-                                        bar(kBarKvFull + s), 64 * h, un.seq_start + j * kKeys,
-                                        kvh);
-                        ++kv_it;
-                    }
-                }
+                for (int j = 1; j < n_kv && ok; ++j)
+                    if (!load_kv(j)) ok = false;
+                if (!ok) break;
                 ++unit_it;
             }
             if (!ok) {
@@ -551,6 +560,10 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     pass_turn();
                     mma_commit(bar(kBarSFull + t));
                     mma_commit(bar(kBarKvEmpty + s));
+                    // Q is free once the unit's last Q.K^T completes: the
+                    // producer loads the next unit's Q during the last
+                    // softmax and P.V instead of after them.
+                    if (n_kv == 1) mma_commit(bar(kBarQEmpty));
                 }
                 for (int j = 0; j < n_kv; ++j) {
                     const uint32_t itv = kv_it + 2u * j + 1u;
@@ -570,9 +583,9 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     mma_commit(bar(more ? kBarSFull + t : kBarOFull + t));
                     mma_commit(bar(kBarKvEmpty + sv));
                     if (more) mma_commit(bar(kBarKvEmpty + sk));
+                    if (j + 2 == n_kv) mma_commit(bar(kBarQEmpty));
                 }
                 if (!ok) break;
-                mma_commit(bar(kBarQEmpty));
                 kv_it += 2u * (uint32_t)n_kv;
                 ++unit_it;
             }
@@ -816,6 +829,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     uint32_t rr[32];
                     tmem_ld32_wait(tO + (uint32_t)ch * 32u, rr);
                     if (valid) {
+                        uint4 pk4[4];
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4) {
                             uint4 pkt;
@@ -823,7 +837,15 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                             pkt.y = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 2]) * inv_l, __uint_as_float(rr[v4 * 8 + 3]) * inv_l);
                             pkt.z = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 4]) * inv_l, __uint_as_float(rr[v4 * 8 + 5]) * inv_l);
                             pkt.w = pack_bf16x2(__uint_as_float(rr[v4 * 8 + 6]) * inv_l, __uint_as_float(rr[v4 * 8 + 7]) * inv_l);
-                            dst[ch * 4 + v4] = pkt;
+                            pk4[v4] = pkt;
+                        }
+                        // 32-byte stores (whole L2 sectors) when o allows it
+                        if (p.o_align32) {
+                            stg256(dst + ch * 4, pk4[0], pk4[1]);
+                            stg256(dst + ch * 4 + 2, pk4[2], pk4[3]);
+                        } else {
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) dst[ch * 4 + v4] = pk4[v4];
                         }
                     }
                 }

@@ -377,6 +377,7 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
     prm->causal = opt.causal;
     prm->out_token_major = opt.out_layout == H3GQA_LAYOUT_TOKEN_MAJOR;
     prm->out_int8 = opt.out_int8;
+    prm->o_align32 = aligned(o, 32) ? 1 : 0;
     prm->n_q_heads = n_q_heads;
     prm->prep_q = prep_q ? 1 : 0;
     prm->stage_rope = (opt.rope_cos != nullptr && hp.unit_tokens <= h3gqa::kRopeMaxTokens) ? 1 : 0;

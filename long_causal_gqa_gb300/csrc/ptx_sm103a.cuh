@@ -113,6 +113,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// 32-byte global store of eight 32-bit words (the address must be 32-byte
+// aligned): one full L2 sector per thread.
+__device__ __forceinline__ void stg256(void *ptr, uint4 a, uint4 b)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(ptr), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z),
+                   "r"(b.w)
+                 : "memory");
+}
+
 // ------------------------------------------------------------ tcgen05 TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
