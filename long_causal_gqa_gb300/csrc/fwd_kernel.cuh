@@ -332,6 +332,11 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
     return ok;
 }
 
+// One instance per output dtype and per Q prologue on/off (p.out_int8 and
+// p.prep_q equal the template arguments), so that a launch carries only the
+// epilogue and prologue code it runs: the code of a unit boundary, run once
+// per unit between the large unrolled softmax blocks, then fetches less.
+template <bool kInt8, bool kPrepQ>
 __global__ void __launch_bounds__(kThreads, 1)
 causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
 {
@@ -547,7 +552,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 if (u >= p.n_units) break;
                 const Unit un = w.at(p, r, gridDim.x, blockIdx.x);
                 const int n_kv = unit_kv_tiles(p, un);
-                if (!wait_poll(bar(p.prep_q ? kBarQReady + t : kBarQFull), unit_it & 1, abort_flag, who, status)) {
+                if (!wait_poll(bar(kPrepQ ? kBarQReady + t : kBarQFull), unit_it & 1, abort_flag, who, status)) {
                     ok = false;
                     break;
                 }
@@ -706,7 +711,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
         const int grid = gridDim.x, cta = blockIdx.x;
         if (unit_of_round(0, grid, cta) < p.n_units) {
             un = w.at(p, 0, grid, cta);
-            if (p.prep_q) ok = prep_q(un, 0);
+            if (kPrepQ) ok = prep_q(un, 0);
         }
         for (long long r = 0; ok; ++r) {
             if (unit_of_round(r, grid, cta) >= p.n_units) break;
@@ -796,7 +801,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             // epilogue run; its rotary table rows are pulled into L1 now.
             ++q_it;
             const bool has_next = unit_of_round(r + 1, grid, cta) < p.n_units;
-            const bool prep_next = p.prep_q && has_next;
+            const bool prep_next = kPrepQ && has_next;
             Unit next_un = un;
             if (prep_next) {
                 next_un = w.at(p, r + 1, grid, cta);
@@ -822,7 +827,7 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             const long long tok_g = (long long)un.seq_start + tok;
             const long long grow = (long long)head * p.total_tokens + tok_g;          // [Hq][T] index
             const long long orow = p.out_token_major ? tok_g * p.n_q_heads + head : grow;
-            if (!p.out_int8) {
+            if (!kInt8) {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + orow * kHeadDim);
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {

@@ -159,9 +159,14 @@ h3gqa_status device_setup(int dev, DeviceState **out, bool again = false)
         *out = &d;
         return d.status;
     }
-    if (cudaFuncSetAttribute(h3gqa::causal_gqa_fwd_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)h3gqa::kSmemBytes) != cudaSuccess) {
+    if (cudaFuncSetAttribute(h3gqa::causal_gqa_fwd_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h3gqa::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(h3gqa::causal_gqa_fwd_kernel<false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h3gqa::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(h3gqa::causal_gqa_fwd_kernel<true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h3gqa::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(h3gqa::causal_gqa_fwd_kernel<true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h3gqa::kSmemBytes) != cudaSuccess) {
         d.ready = false;
         return H3GQA_ERR_CUDA;
     }
@@ -387,16 +392,22 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
     prm->norm_eps = opt.norm_eps;
     prm->scale_log2 = scale * 1.4426950408889634f;
     const int grid = fill_schedule(hp, kv_begin, ds->sm_count, prm);
-    h3gqa::causal_gqa_fwd_kernel<<<(unsigned)grid, h3gqa::kThreads, h3gqa::kSmemBytes,
-                                   reinterpret_cast<cudaStream_t>(stream)>>>(*prm);
+    // the instance for this call's output dtype and Q prologue
+    void (*kernel)(const FwdParams) =
+        prm->out_int8 ? (prm->prep_q ? h3gqa::causal_gqa_fwd_kernel<true, true>
+                                     : h3gqa::causal_gqa_fwd_kernel<true, false>)
+                      : (prm->prep_q ? h3gqa::causal_gqa_fwd_kernel<false, true>
+                                     : h3gqa::causal_gqa_fwd_kernel<false, false>);
+    kernel<<<(unsigned)grid, h3gqa::kThreads, h3gqa::kSmemBytes,
+             reinterpret_cast<cudaStream_t>(stream)>>>(*prm);
     cudaError_t err = cudaGetLastError();
     if (err == cudaErrorInvalidValue || err == cudaErrorLaunchOutOfResources) {
         // The kernel's shared-memory attribute is per context: after a device
         // reset it is gone although this table still says ready. Set the
         // device up again and launch once more.
         if (device_setup(dev, &ds, true) == H3GQA_OK) {
-            h3gqa::causal_gqa_fwd_kernel<<<(unsigned)grid, h3gqa::kThreads, h3gqa::kSmemBytes,
-                                           reinterpret_cast<cudaStream_t>(stream)>>>(*prm);
+            kernel<<<(unsigned)grid, h3gqa::kThreads, h3gqa::kSmemBytes,
+                     reinterpret_cast<cudaStream_t>(stream)>>>(*prm);
             err = cudaGetLastError();
         }
     }
