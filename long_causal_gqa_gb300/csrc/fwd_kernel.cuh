@@ -55,13 +55,12 @@ constexpr uint32_t kTileBytes = 2 * kSubTileBytes;     // 128 rows x 128 bf16
 constexpr uint32_t kQOff = 0;                          // two query tiles
 constexpr uint32_t kKvOff = kQOff + 2 * kTileBytes;
 constexpr uint32_t kRopeOff = kKvOff + kStages * kTileBytes;   // cos rows, then sin rows, of one unit
-constexpr uint32_t kRopeRowBytes = kHeadDim / 2 * 4;           // 64 fp32 per token
 constexpr int kRopeMaxTokens = 32;                             // staged when a unit has <= 32 tokens (G >= 8)
-// Staged rows are 16 bytes apart beyond their length, so the eight tokens a
-// quarter-warp reads at one column fall in eight different bank groups (with
-// a 256-byte stride they would all hit the same four banks).
-constexpr uint32_t kRopeStride = kRopeRowBytes + 16;
-constexpr uint32_t kRopeBytes = 2 * kRopeMaxTokens * kRopeStride;
+// Each table's 32 rows of 64 fp32 come in as two TMA boxes of 32 rows x 32
+// floats (128 bytes) in the 128-byte-swizzled layout, so the eight tokens a
+// quarter-warp reads at one column fall in eight different bank groups.
+constexpr uint32_t kRopeHalfBytes = kRopeMaxTokens * 128;      // one box
+constexpr uint32_t kRopeBytes = 2 * 2 * kRopeHalfBytes;        // cos, sin x two halves
 constexpr uint32_t kBarOff = kRopeOff + kRopeBytes;
 // barrier slots
 constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + kStages,
@@ -70,7 +69,8 @@ constexpr int kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + k
 constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag, [2..3] MMA turn counters
 constexpr uint32_t kSchedOff = kMiscOff + 16;          // softmax threads' unit-schedule state, one slot each
 constexpr uint32_t kSchedSlotBytes = 24;
-constexpr uint32_t kSmemBytes = kSchedOff + 256 * kSchedSlotBytes + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kQNormWOff = kSchedOff + 256 * kSchedSlotBytes;   // the Q norm weight, bf16 [128]
+constexpr uint32_t kSmemBytes = kQNormWOff + kHeadDim * 2 + 1024;     // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if the max grew by > 2^8
 #ifndef H3GQA_WAIT_NS
@@ -88,6 +88,8 @@ struct FwdParams {
     CUtensorMap map_q;      // q [Hq][T][128], box {64, tile_tokens, tile_heads}
     CUtensorMap map_k;      // k [Hkv][T][128], box {64, 128, 1}
     CUtensorMap map_v;      // v [Hkv][T][128], box {64, 128, 1}
+    CUtensorMap map_cos;    // rotary cos [T][64] fp32, box {32, 32} (staged rotary only)
+    CUtensorMap map_sin;    // rotary sin, likewise
     void *o;                // bf16 (or int8 codes) [Hq][T][128] or [T][Hq][128]
     float *lse;             // fp32 [Hq][T]
     float *o_scale;         // int8 output only: one fp32 scale per (token, head) row
@@ -354,6 +356,13 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
     const int lane = threadIdx.x & 31;
     unsigned int *const status = p.status;
 
+    if (kPrepQ && p.q_norm_w != nullptr && threadIdx.x < kHeadDim * 2 / 16) {
+        // The Q norm weight is read by every row of every unit's Q tile: one
+        // copy in shared memory (global loads would mostly miss the small L1
+        // that shared memory leaves and sit on the transform's critical path).
+        reinterpret_cast<uint4 *>(smem + kQNormWOff)[threadIdx.x] =
+            __ldg(reinterpret_cast<const uint4 *>(p.q_norm_w) + threadIdx.x);
+    }
     if (p.tile_rows < kRows) {
         // Query tiles with unused MMA rows: TMA never writes those rows, so
         // they are zeroed once here (their scores stay finite; every MMA row
@@ -399,6 +408,10 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             tma_prefetch_map(&p.map_q);
             tma_prefetch_map(&p.map_k);
             tma_prefetch_map(&p.map_v);
+            if (p.stage_rope) {
+                tma_prefetch_map(&p.map_cos);
+                tma_prefetch_map(&p.map_sin);
+            }
             Schedule w;
             w.init(p);
             uint32_t kv_it = 0, unit_it = 0;
@@ -434,21 +447,18 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                 // buffer, so it is in flight while the last unit finishes.
                 if (!load_kv(0)) { ok = false; break; }
                 if (!wait_poll(bar(kBarQEmpty), (unit_it & 1) ^ 1, abort_flag, 1u, status)) { ok = false; break; }
-                uint32_t rope_bytes = 0;
-                const long long tok0 = (long long)un.seq_start + tb;
-                if (p.stage_rope) {
-                    const long long rows = min((long long)p.unit_tokens, p.total_tokens - tok0);
-                    rope_bytes = (uint32_t)rows * kRopeRowBytes;
-                }
-                mbar_arrive_expect_tx(bar(kBarQFull), p.q_tx_bytes + 2 * rope_bytes);
+                const int tok0 = un.seq_start + tb;
+                mbar_arrive_expect_tx(bar(kBarQFull), p.q_tx_bytes + (p.stage_rope ? kRopeBytes : 0u));
                 last_q_parity = unit_it & 1;
-                // one copy per token row (cos, then sin), into the padded rows
-                for (uint32_t rr = 0; rr < rope_bytes / kRopeRowBytes; ++rr) {
-                    const long long tr = tok0 + rr;
-                    bulk_load(sbase + kRopeOff + rr * kRopeStride, p.rope_cos + tr * (kHeadDim / 2), kRopeRowBytes,
-                              bar(kBarQFull));
-                    bulk_load(sbase + kRopeOff + kRopeBytes / 2 + rr * kRopeStride, p.rope_sin + tr * (kHeadDim / 2),
-                              kRopeRowBytes, bar(kBarQFull));
+                if (p.stage_rope) {
+                    // the unit's rotary rows: 32 rows of each table (rows past
+                    // T read as zero), two 128-byte halves each
+                    for (int h = 0; h < 2; ++h) {
+                        tma_load_2d(sbase + kRopeOff + (uint32_t)h * kRopeHalfBytes, &p.map_cos, bar(kBarQFull),
+                                    32 * h, tok0);
+                        tma_load_2d(sbase + kRopeOff + (uint32_t)(2 + h) * kRopeHalfBytes, &p.map_sin,
+                                    bar(kBarQFull), 32 * h, tok0);
+                    }
                 }
                 for (int t = 0; t < 2; ++t)
                     for (int h = 0; h < 2; ++h)
@@ -634,18 +644,25 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                         f[2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
                     }
                 };
+                // the row is read from shared memory once (all 16 chunks in
+                // flight), normalised and rotated from registers
+                uint4 qa[8], qb[8];
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    qa[cc] = *chunk(0, cc);
+                    qb[cc] = *chunk(1, cc);
+                }
                 float rs = 1.0f;
                 if (p.q_norm_w != nullptr) {
                     float ss = 0.f;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                    for (int cc = 0; cc < 8; ++cc) {
+                        float f[8], g[8];
+                        unpack(qa[cc], f);
+                        unpack(qb[cc], g);
 #pragma unroll
-                        for (int cc = 0; cc < 8; ++cc) {
-                            float f[8];
-                            unpack(*chunk(h, cc), f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-                        }
+                        for (int e = 0; e < 8; ++e) ss = fmaf(g[e], g[e], fmaf(f[e], f[e], ss));
+                    }
                     rs = rsqrtf(ss * (1.0f / kHeadDim) + p.norm_eps);
                 }
                 // element i of the first half pairs with element i + 64 for the
@@ -653,11 +670,11 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
                     float a[8], b[8];
-                    unpack(*chunk(0, cc), a);
-                    unpack(*chunk(1, cc), b);
+                    unpack(qa[cc], a);
+                    unpack(qb[cc], b);
                     if (p.q_norm_w != nullptr) {
-                        const uint4 wa = __ldg(reinterpret_cast<const uint4 *>(p.q_norm_w) + cc);
-                        const uint4 wb = __ldg(reinterpret_cast<const uint4 *>(p.q_norm_w) + 8 + cc);
+                        const uint4 wa = reinterpret_cast<const uint4 *>(smem + kQNormWOff)[cc];
+                        const uint4 wb = reinterpret_cast<const uint4 *>(smem + kQNormWOff)[8 + cc];
                         float fa[8], fb[8];
                         unpack(wa, fa);
                         unpack(wb, fb);
@@ -670,10 +687,16 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
                     if (p.rope_cos != nullptr) {
                         float4 c0, c1, s0, s1;
                         if (p.stage_rope) {
-                            const float4 *cs4 = reinterpret_cast<const float4 *>(
-                                smem + kRopeOff + (uint32_t)(t * p.tile_tokens + tok_in_tile) * kRopeStride) + 2 * cc;
-                            const float4 *sn4 = cs4 + kRopeBytes / 2 / 16;
-                            c0 = cs4[0]; c1 = cs4[1]; s0 = sn4[0]; s1 = sn4[1];
+                            // floats 8cc..8cc+7: half cc/4, 16-byte chunks 2(cc%4) and 2(cc%4)+1
+                            // of row ur, in the swizzled layout TMA wrote
+                            const uint32_t ur = (uint32_t)(t * p.tile_tokens + tok_in_tile);
+                            const uint32_t rb = kRopeOff + (uint32_t)(cc >> 2) * kRopeHalfBytes + ur * 128u;
+                            const uint32_t k0 = (uint32_t)((2 * (cc & 3)) ^ (ur & 7)) << 4;
+                            const uint32_t k1 = (uint32_t)((2 * (cc & 3) + 1) ^ (ur & 7)) << 4;
+                            c0 = *reinterpret_cast<const float4 *>(smem + rb + k0);
+                            c1 = *reinterpret_cast<const float4 *>(smem + rb + k1);
+                            s0 = *reinterpret_cast<const float4 *>(smem + rb + 2 * kRopeHalfBytes + k0);
+                            s1 = *reinterpret_cast<const float4 *>(smem + rb + 2 * kRopeHalfBytes + k1);
                         } else {
                             const float4 *cs4 = reinterpret_cast<const float4 *>(p.rope_cos + tokg * (kHeadDim / 2) + 8 * cc);
                             const float4 *sn4 = reinterpret_cast<const float4 *>(p.rope_sin + tokg * (kHeadDim / 2) + 8 * cc);

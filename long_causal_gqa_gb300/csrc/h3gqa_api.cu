@@ -232,6 +232,19 @@ int fill_schedule(const HostPlan &hp, int kv_begin, int sm_count, FwdParams *prm
     return grid;
 }
 
+// A rotary table fp32 [T][64] as a 2-D map with {32, 32} boxes (32 rows of
+// one 128-byte half) and the 128-byte swizzle the Q prologue reads.
+bool encode_map_rope(CUtensorMap *map, const float *base, long long T)
+{
+    cuuint64_t dims[2] = {(cuuint64_t)h3gqa::kHeadDim / 2, (cuuint64_t)T};
+    cuuint64_t strides[1] = {(cuuint64_t)h3gqa::kHeadDim / 2 * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)h3gqa::kRopeMaxTokens};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // [a, a + na) and [b, b + nb) share a byte
@@ -386,6 +399,11 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
     prm->n_q_heads = n_q_heads;
     prm->prep_q = prep_q ? 1 : 0;
     prm->stage_rope = (opt.rope_cos != nullptr && hp.unit_tokens <= h3gqa::kRopeMaxTokens) ? 1 : 0;
+    if (prm->stage_rope && (!encode_map_rope(&prm->map_cos, opt.rope_cos, T) ||
+                            !encode_map_rope(&prm->map_sin, opt.rope_sin, T))) {
+        delete prm;
+        return H3GQA_ERR_CUDA;
+    }
     prm->q_norm_w = static_cast<const uint16_t *>(opt.q_norm_weight);
     prm->rope_cos = opt.rope_cos;
     prm->rope_sin = opt.rope_sin;
