@@ -96,7 +96,9 @@ typedef enum {
  *   stream      stream to queue the kernel on.
  *
  * Returns H3GQA_OK once the kernel is queued (T = 0 queues nothing).
- * Invalid arguments return before any CUDA call. There is no limit on the
+ * Invalid arguments return before any CUDA call; an o that shares a byte
+ * with q, k, v or lse is one (o is written while other work units of the
+ * same call still read the inputs). There is no limit on the
  * sequence length other than T < 2^31 - 256 (TMA coordinates are int32).
  * Rows of o/lse are written only for tokens inside some sequence, i.e. all
  * of [0, T).
@@ -189,8 +191,9 @@ typedef struct {
  * h3gqa_causal_fwd; in addition an options value outside the ranges above,
  * out_int8 without a valid o_scale, a misaligned prologue pointer, rope_cos
  * without rope_sin (or the reverse), a prepared k without k_out, a k_out
- * that overlaps q, v or part of k, a misaligned status word or a head shard
- * outside [0, n_kv_heads) returns H3GQA_ERR_INVALID_ARG. lse is always
+ * that overlaps q, v or part of k, an o that overlaps k_out or o_scale, a
+ * misaligned status word or a head shard outside [0, n_kv_heads) returns
+ * H3GQA_ERR_INVALID_ARG. lse is always
  * [Hq][T].
  */
 h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v,

@@ -250,6 +250,21 @@ def check_tensors(q, k, v, cu_seqlens, q_norm_weight=None, k_norm_weight=None, r
     return hq, hkv, T, d
 
 
+def check_output_disjoint(o, **others):
+    """o is written while other units still read the inputs, so it may share
+    no byte with q, k, v, lse, k_out or o_scale."""
+    def span(t):
+        return t.data_ptr(), t.data_ptr() + t.numel() * t.element_size()
+    if o is None or o.numel() == 0:
+        return
+    a0, a1 = span(o)
+    for name, t in others.items():
+        if t is not None and t.numel() > 0:
+            b0, b1 = span(t)
+            if a0 < b1 and b0 < a1:
+                raise ValueError("o must not overlap %s" % name)
+
+
 def _check_cuda(*tensors):
     for t in tensors:
         if t is not None and not t.is_cuda:
@@ -304,6 +319,8 @@ def attention_fwd(q, k, v, cu_seqlens, scale=None, causal=True, token_major=Fals
     prep_k = k_norm_weight is not None or rope_cos is not None
     if prep_k and k_out is None:
         k_out = torch.empty_like(k)
+    check_output_disjoint(o, q=q, k=k, v=v, lse=lse, k_out=k_out if prep_k else None,
+                          o_scale=o_scale)
     kv_begin, kv_count = kv_heads if kv_heads is not None else (0, 0)
     status = torch.zeros(1, dtype=torch.int32, device=q.device) if check else None
     ptr = lambda t: t.data_ptr() if t is not None else None

@@ -353,6 +353,13 @@ h3gqa_status h3gqa_attention_fwd(const void *q, const void *k, const void *v, vo
             (overlaps(opt.k_out, kb, q, qb) || overlaps(opt.k_out, kb, v, kb) ||
              (opt.k_out != k && overlaps(opt.k_out, kb, k, kb))))
             return H3GQA_ERR_INVALID_ARG;
+        // o is written while other units still read q, k and v
+        const unsigned long long ob = (opt.out_int8 ? 1ull : 2ull) * n_q_heads * T * head_dim;
+        const unsigned long long lb = 4ull * n_q_heads * T;
+        if (T > 0 && (overlaps(o, ob, q, qb) || overlaps(o, ob, k, kb) || overlaps(o, ob, v, kb) ||
+                      overlaps(o, ob, lse, lb) || (prep_k && overlaps(o, ob, opt.k_out, kb)) ||
+                      (opt.out_int8 && overlaps(o, ob, opt.o_scale, lb))))
+            return H3GQA_ERR_INVALID_ARG;
     }
     if (hp.n_units == 0) return H3GQA_OK;
 

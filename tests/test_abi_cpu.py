@@ -260,6 +260,41 @@ def test_k_out_overlap_rejected_before_cuda(lib):
             H3GQA_ERR_INVALID_ARG, hex(k_out)
 
 
+def test_o_overlap_rejected_before_cuda(lib):
+    """o may share no byte with q, k, v, lse, k_out or o_scale (it is written
+    while other units still read the inputs). o is 64*64*128*2 bytes here,
+    lse 64*64*4."""
+    q, k, v, o, lse = 1 << 24, 1 << 26, 1 << 27, 1 << 28, 1 << 29
+    base = dict(q_ptr=q, k_ptr=k, v_ptr=v, o_ptr=o, lse_ptr=lse,
+                cu_seqlens=[0, 64], n_q_heads=64, n_kv_heads=8, head_dim=128, scale=0.088)
+    obytes, lbytes, kbytes = 64 * 64 * 128 * 2, 64 * 64 * 4, 8 * 64 * 128 * 2
+    for bad_o in (q, q + 16, k - obytes + 16, v + kbytes - 16, lse - obytes + 16, lse + lbytes - 16):
+        assert binding.h3gqa_attention_fwd(check=False, **dict(base, o_ptr=bad_o)) == \
+            H3GQA_ERR_INVALID_ARG, hex(bad_o)
+    k_out = 1 << 25
+    opts = binding.make_options(k_norm_ptr=1 << 20, k_out_ptr=k_out)
+    assert binding.h3gqa_attention_fwd(options=opts, check=False,
+                                       **dict(base, o_ptr=k_out + 16)) == H3GQA_ERR_INVALID_ARG
+    o_scale = 1 << 30
+    opts = binding.make_options(out_int8=True, o_scale_ptr=o_scale)
+    assert binding.h3gqa_attention_fwd(options=opts, check=False,
+                                       **dict(base, o_ptr=o_scale - 64 * 64 * 128 + 16)) == \
+        H3GQA_ERR_INVALID_ARG
+
+
+def test_o_overlap_rejected_in_the_binding():
+    import torch
+    buf = torch.zeros(4 * 40 * 128 * 4, dtype=torch.bfloat16)
+    q = buf[: 8 * 40 * 128].view(8, 40, 128)
+    o_bad = buf[4 * 40 * 128: 12 * 40 * 128].view(8, 40, 128)
+    o_ok = buf[8 * 40 * 128: 16 * 40 * 128].view(8, 40, 128)
+    with pytest.raises(ValueError):
+        binding.check_output_disjoint(o_bad, q=q)
+    with pytest.raises(ValueError):
+        binding.check_output_disjoint(q, q=q)
+    binding.check_output_disjoint(o_ok, q=q, lse=None)
+
+
 def test_shard_heads_partition():
     """Contiguous head ranges: every head exactly once, sizes within one."""
     for n in (1, 3, 8, 64):
