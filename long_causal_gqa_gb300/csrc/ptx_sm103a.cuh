@@ -103,6 +103,33 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// The same load with an L2 cache policy (from l2_policy_*).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int c0, int c1, int c2, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar),
+          "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+// L2 cache policies: lines fetched under evict_last are kept over others,
+// evict_first lines are the first to go.
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 2-D tiled load into shared memory, completion signalled on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1)
 {
@@ -132,6 +159,16 @@ __device__ __forceinline__ void stg256(void *ptr, uint4 a, uint4 b)
                    "r"(b.w)
                  : "memory");
 }
+
+// The same store with an L2 cache policy.
+__device__ __forceinline__ void stg256_hint(void *ptr, uint4 a, uint4 b, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+                 ::"l"(ptr), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z),
+                   "r"(b.w), "l"(policy)
+                 : "memory");
+}
+
 
 // ------------------------------------------------------------ tcgen05 TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
