@@ -34,16 +34,18 @@ def dev():
     return torch.device("cuda:0")
 
 
-def run_gpu(x, hq, hkv, scale, dev, stream=None, as_numpy=True):
+def run_gpu(x, hq, hkv, scale, dev, stream=None, as_numpy=True, o_shift=0):
     """Runs the library with guard regions around o and lse; returns numpy
     (o fp64 [Hq,T,D], lse fp64 [Hq,T]), or the CPU tensors (o bf16, lse fp32)
-    when as_numpy is False (large outputs: convert only sampled rows)."""
+    when as_numpy is False (large outputs: convert only sampled rows).
+    o_shift moves o by that many bf16 elements from its 32-byte-aligned
+    place (8: o is 16-byte but not 32-byte aligned)."""
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     T, d = q.shape[1], q.shape[2]
     n_o, n_l = hq * T * d, hq * T
-    o_buf = torch.full((n_o + 2 * GUARD,), O_SENTINEL, dtype=torch.int16, device=dev)
+    o_buf = torch.full((n_o + 2 * GUARD + o_shift,), O_SENTINEL, dtype=torch.int16, device=dev)
     l_buf = torch.full((n_l + 2 * GUARD,), LSE_SENTINEL, dtype=torch.int32, device=dev)
-    o = o_buf[GUARD:GUARD + n_o].view(torch.bfloat16).view(hq, T, d)
+    o = o_buf[GUARD + o_shift:GUARD + o_shift + n_o].view(torch.bfloat16).view(hq, T, d)
     lse = l_buf[GUARD:GUARD + n_l].view(torch.float32).view(hq, T)
     s = stream or torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
@@ -133,6 +135,19 @@ def test_any_group_size_bidirectional(dev, hq, hkv):
     assert_close(o.float().cpu().numpy().astype(np.float64),
                  lse.cpu().numpy().astype(np.float64), ref_o, ref_lse,
                  "bidirectional hq=%d hkv=%d" % (hq, hkv))
+
+
+def test_o_only_16_byte_aligned(dev):
+    """o 16-byte but not 32-byte aligned takes the 16-byte store path of the
+    epilogue: same bits as the aligned call, within the bar of the oracle,
+    guards untouched, on ragged sequences that leave partial tiles."""
+    hq, hkv, scale = 16, 2, 128 ** -0.5
+    x = make_inputs((300, 0, 129, 5, 700), hq, hkv, 128, 4711)
+    o16, lse16 = run_gpu(x, hq, hkv, scale, dev, o_shift=8)
+    o32, lse32 = run_gpu(x, hq, hkv, scale, dev)
+    assert np.array_equal(o16, o32) and np.array_equal(lse16, lse32)
+    ref_o, ref_lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv, scale)
+    assert_close(o16, lse16, ref_o, ref_lse, "(o 16-byte aligned)")
 
 
 def test_workload_s512_full(dev):
