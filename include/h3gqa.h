@@ -128,7 +128,9 @@ h3gqa_status h3gqa_causal_fwd(const void *q, const void *k, const void *v,
  * out_int8 = 1 writes o as int8 codes with one fp32 scale per (token, head)
  * row of head_dim values: scale = max|o_row| / 127 (1 for an all-zero row),
  * code = round-to-nearest-even(o / scale) clamped to [-127, 127], so
- * o ~= code * scale. o then holds 1 byte per element (16-byte aligned) and
+ * o ~= code * scale. A row whose max|o_row| is at most 3.75e-37 (where
+ * 127 / max|o_row| would overflow fp32) gets all-zero codes, its scale still
+ * max|o_row| / 127. o then holds 1 byte per element (16-byte aligned) and
  * o_scale is laid out like o without the last dimension.
  */
 typedef enum {

@@ -913,21 +913,30 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
 #pragma unroll
                 for (int i = 0; i < kHeadDim; ++i) amax = fmaxf(amax, fabsf(x[i]));
                 const float qscale = amax > 0.f ? amax / 127.0f : 1.0f;
-                const float inv_q = amax > 0.f ? 127.0f / amax : 0.0f;
+                // 127 / max|o| is finite for max|o| > 3.75e-37; a row below
+                // that gets all-zero codes (within 3.75e-37 of o)
+                const float inv_q = amax > 3.75e-37f ? 127.0f / amax : 0.0f;
                 if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<int8_t *>(p.o) + orow * kHeadDim);
+                    // t = x * inv_q lies in [-127, 127] up to the product's
+                    // rounding (it cannot reach 127.5), so adding 1.5 * 2^23
+                    // rounds it to the nearest integer, ties to even, and
+                    // leaves that integer's two's-complement low byte in the
+                    // low byte of the sum's bits: the same code as converting
+                    // t to an integer, on the FMA pipe instead of the
+                    // conversion unit. Separate multiply and add (never
+                    // contracted) keep t rounded to fp32 first.
+                    constexpr float kRound = 12582912.0f;
 #pragma unroll
                     for (int v4 = 0; v4 < kHeadDim / 16; ++v4) {
                         uint32_t w4[4];
 #pragma unroll
                         for (int wi = 0; wi < 4; ++wi) {
-                            uint32_t word = 0;
+                            uint32_t b[4];
 #pragma unroll
-                            for (int bi = 0; bi < 4; ++bi) {
-                                const int c = __float2int_rn(fminf(fmaxf(x[v4 * 16 + wi * 4 + bi] * inv_q, -127.f), 127.f));
-                                word |= ((uint32_t)c & 0xFFu) << (8 * bi);
-                            }
-                            w4[wi] = word;
+                            for (int bi = 0; bi < 4; ++bi)
+                                b[bi] = __float_as_uint(__fadd_rn(__fmul_rn(x[v4 * 16 + wi * 4 + bi], inv_q), kRound));
+                            w4[wi] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
                         }
                         dst[v4] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }

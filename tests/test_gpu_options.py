@@ -77,6 +77,23 @@ def test_token_major_is_the_transposed_head_major(dev, causal):
     assert torch.equal(lse_t, lse_h)
 
 
+def test_int8_rows_too_small_to_scale(dev):
+    """Rows whose max|o| is at most 3.75e-37 (127 / max|o| would overflow
+    fp32) are written as all-zero codes with scale max|o| / 127: no NaN or
+    saturated codes. Every o row is a convex combination of v rows, so with
+    |v| < 3.7e-37 every row is such a row, whatever the tensor cores do with
+    the denormal products; the LSE does not depend on v."""
+    x = make_inputs((300, 77), 16, 2, 128, seed=43)
+    x["v"] = (x["v"].float() * 5e-38).to(torch.bfloat16)
+    assert float(x["v"].float().abs().max()) < 3.7e-37
+    codes, lse, scale = _run(x, dev, causal=True, token_major=False, out_int8=True)
+    _, lse_bf, _ = _run(x, dev, causal=True, token_major=False)
+    assert int(codes.abs().max()) == 0
+    assert torch.isfinite(scale).all() and float(scale.min()) >= 0.0
+    assert float(scale.max()) <= 3.75e-37 / 127.0
+    assert torch.equal(lse, lse_bf)
+
+
 @pytest.mark.parametrize("token_major,causal", [(False, True), (True, True), (True, False)])
 def test_int8_output(dev, token_major, causal):
     x = make_inputs((640, 77), 64, 8, 128, seed=42)
