@@ -97,3 +97,44 @@ def test_cuda_graph_capture_and_replay(dev):
         torch.cuda.synchronize(dev)
         assert binding.h3gqa_sync_and_check(0) == binding.H3GQA_OK
         assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
+def test_cuda_graph_with_prologue_and_int8(dev):
+    """The prologue's two launches (K pass, then attention) and the int8
+    token-major epilogue, captured in one graph, replay to the eager result
+    bit for bit: codes, scales, LSE and the prepared keys."""
+    from long_causal_gqa_gb300.inputs import norm_weights, rope_tables
+    seqlens = (1500, 0, 333)
+    x = make_inputs(seqlens, 64, 8, 128, seed=82)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    wq, wk = (t.to(dev) for t in norm_weights(128, 82))
+    cos, sin = (t.to(dev) for t in rope_tables(seqlens, 128))
+    kw = dict(q_norm_weight=wq, k_norm_weight=wk, rope_cos=cos, rope_sin=sin,
+              token_major=True, out_int8=True)
+    o_ref, lse_ref, sc_ref = binding.attention_fwd(q, k, v, x["cu_seqlens"], SCALE, **kw)
+    k_ref = torch.empty_like(k)
+    binding.attention_fwd(q, k, v, x["cu_seqlens"], SCALE, k_out=k_ref, **kw)
+    T = q.shape[1]
+    o = torch.empty((T, 64, 128), dtype=torch.int8, device=dev)
+    lse = torch.empty((64, T), dtype=torch.float32, device=dev)
+    sc = torch.empty((T, 64), dtype=torch.float32, device=dev)
+    k_out = torch.empty_like(k)
+    opts = binding.make_options(True, binding.H3GQA_LAYOUT_TOKEN_MAJOR, True, sc.data_ptr(), 0,
+                                wq.data_ptr(), wk.data_ptr(), cos.data_ptr(), sin.data_ptr(),
+                                k_out.data_ptr())
+    stream = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        st = binding.h3gqa_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), x["cu_seqlens"], 64, 8, 128, SCALE,
+                                         options=opts, stream=torch.cuda.current_stream(dev).cuda_stream,
+                                         check=False)
+        assert st == binding.H3GQA_OK
+    for _ in range(2):
+        for t in (o, lse, sc, k_out):
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        assert binding.h3gqa_sync_and_check(0) == binding.H3GQA_OK
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref) and torch.equal(sc, sc_ref)
+        assert torch.equal(k_out, k_ref)
