@@ -24,8 +24,8 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _case(seqlens, seed, use_qn, use_kn, use_rope, causal, dev, in_place=False):
-    x = make_inputs(seqlens, 64, 8, 128, seed)
+def _case(seqlens, seed, use_qn, use_kn, use_rope, causal, dev, in_place=False, hq=64, hkv=8):
+    x = make_inputs(seqlens, hq, hkv, 128, seed)
     wq, wk = norm_weights(128, seed)
     cos, sin = rope_tables(seqlens, 128)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
@@ -53,7 +53,7 @@ def _case(seqlens, seed, use_qn, use_kn, use_rope, causal, dev, in_place=False):
         k_att = orc.to_bf16(k_ref)
     else:
         k_att = x["k"]
-    ro, rl = orc.causal_gqa(orc.to_bf16(q_ref), k_att, x["v"], x["cu_seqlens"], 64, 8, SCALE,
+    ro, rl = orc.causal_gqa(orc.to_bf16(q_ref), k_att, x["v"], x["cu_seqlens"], hq, hkv, SCALE,
                             causal=causal)
     o64 = o.float().cpu().numpy().astype(np.float64)
     assert np.isfinite(o64).all()
@@ -74,3 +74,12 @@ def test_prologue_bidirectional_and_in_place(dev):
 
 def test_prologue_long_sequence(dev):
     _case((2100,), 63, True, True, True, True, dev)
+
+
+@pytest.mark.parametrize("hq,hkv,causal", [(256, 1, True), (256, 2, False), (131, 1, True)])
+def test_prologue_tiles_beyond_one_group(dev, hq, hkv, causal):
+    """Group sizes above 128 (a KV head's query heads span several tiles:
+    G = 256 packs 128 heads x 1 token per tile, with the rotary rows staged
+    beside Q) and a prime G = 131 (one head x 128 tokens per tile, rotary
+    rows read from global memory), with every part of the prologue."""
+    _case((70, 0, 9), 64 + hq + hkv, True, True, True, causal, dev, hq=hq, hkv=hkv)
