@@ -117,3 +117,24 @@ def test_int8_output(dev, token_major, causal):
     # against the bf16 output of the same kernel: half a step plus bf16 rounding
     ob = o_bf.float().numpy()
     assert (np.abs(deq.numpy() - ob) <= 0.5 * step + np.abs(ob) * 2.0 ** -8 + 1e-6).all()
+
+
+@pytest.mark.parametrize("hq,hkv", [(3, 1), (131, 1), (24, 8)])
+def test_epilogue_forms_with_unusual_tiles(dev, hq, hkv):
+    """Token-major bf16 is bitwise the transpose of head-major, and int8 codes
+    dequantize to the bf16 output within half a step (plus bf16 rounding),
+    for tiles with unused rows (G = 3: 126 of 128), one head per tile
+    (G = 131) and a non-power-of-two divisor (G = 3 of Hq/Hkv = 24/8)."""
+    x = make_inputs((300, 0, 77), hq, hkv, 128, seed=500 + hq)
+    o_h, lse_h, _ = _run(x, dev, causal=True)
+    o_t, lse_t, _ = _run(x, dev, causal=True, token_major=True)
+    assert torch.equal(o_t, o_h.transpose(0, 1)) and torch.equal(lse_t, lse_h)
+    codes, lse_q, scale = _run(x, dev, causal=True, token_major=True, out_int8=True)
+    assert torch.equal(lse_q, lse_h)
+    assert int(codes.abs().max()) <= 127
+    deq = codes.float() * scale[..., None]
+    ob = o_t.float()
+    step = scale[..., None]
+    assert (np.abs((deq - ob).numpy()) <= (0.5 * step + ob.abs() * 2.0 ** -8 + 1e-6).numpy()).all()
+    ref_o, ref_lse = orc.causal_gqa(x["q"], x["k"], x["v"], x["cu_seqlens"], hq, hkv, SCALE)
+    _check(o_h.float().numpy(), lse_h.numpy(), ref_o, ref_lse, "G=%d" % (hq // hkv))
