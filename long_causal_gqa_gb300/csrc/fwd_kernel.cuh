@@ -868,7 +868,9 @@ causal_gqa_fwd_kernel(const __grid_constant__ FwdParams p)
             const long long orow = p.out_token_major ? tok_g * p.n_q_heads + head : grow;
             if (!kInt8) {
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.o) + orow * kHeadDim);
-#pragma unroll
+                // a rolled loop: this code runs once per unit, and less of it
+                // is fetched at the unit boundary (paired: +0.1 to +0.9%)
+#pragma unroll 1
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t rr[32];
                     tmem_ld32_wait(tO + (uint32_t)ch * 32u, rr);
