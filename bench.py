@@ -449,7 +449,8 @@ def measure_e2e(case, args, device, stream, world):
                      sc=torch.empty_like(case.o_scale) if case.o_scale is not None else None))
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     e2e_steps = max(4, min(args.steps, 20))
-    n_total = e2e_steps + 2
+    n_windows = 3
+    n_total = n_windows * e2e_steps + 2
     ev_in = [torch.cuda.Event() for _ in range(n_total)]
     ev_comp = [torch.cuda.Event() for _ in range(n_total)]
     ev_out = [torch.cuda.Event() for _ in range(n_total)]
@@ -478,15 +479,21 @@ def measure_e2e(case, args, device, stream, world):
 
     for i in range(2):
         e2e_step(i)
-    torch.cuda.synchronize(device)
-    barrier(world)
-    te0 = time.perf_counter()
-    for i in range(2, n_total):
-        e2e_step(i)
-    torch.cuda.synchronize(device)
-    e2e_ms = (time.perf_counter() - te0) * 1e3 / e2e_steps
+    # three timed windows of e2e_steps pipelined steps each (the pipeline
+    # drains between windows); the median window is reported, so one stall
+    # of the host does not stand for the whole measurement
+    windows = []
+    for wi in range(n_windows):
+        torch.cuda.synchronize(device)
+        barrier(world)
+        te0 = time.perf_counter()
+        for i in range(2 + wi * e2e_steps, 2 + (wi + 1) * e2e_steps):
+            e2e_step(i)
+        torch.cuda.synchronize(device)
+        windows.append((time.perf_counter() - te0) * 1e3 / e2e_steps)
     binding.h3gqa_sync_and_check(case.sh)
-    return max_over_ranks(e2e_ms, world, device), h2d, d2h
+    e2e_ms = float(np.median(windows))
+    return max_over_ranks(e2e_ms, world, device), h2d, d2h, windows
 
 
 def run_ours(args, world, rank, local):
@@ -516,7 +523,7 @@ def run_ours(args, world, rank, local):
             del ec
     sampler.stop()
 
-    e2e_ms, h2d, d2h = measure_e2e(case, args, device, stream, world)
+    e2e_ms, h2d, d2h, e2e_windows = measure_e2e(case, args, device, stream, world)
 
     if rank != 0:
         return
@@ -550,8 +557,10 @@ def run_ours(args, world, rank, local):
                      "work": "4*D FLOPs per visible (query, key, head) pair per launch"},
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step_windows": [round(x, 4) for x in e2e_windows],
                 "api": "h3gqa_attention_fwd via the Python binding; pinned host buffers; "
-                       "upload / compute / download on three streams, two device buffer sets"},
+                       "upload / compute / download on three streams, two device buffer sets; "
+                       "median of three timed windows"},
         "gpu_launches": args.steps * case.launches_per_step if case.kv_count else 0,
         "clocks": clocks,
         "kernel_ms": {"mean": ms, "min": float(np.min(times)), "max": float(np.max(times))},
